@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark of the ResidualKV cache-write path (and its sparse read) on GB300.
+
+One step = the whole hot path over the Llama-3.1-8B KV-shape workload: for all 32
+layers x 8192 tokens, build the reference pool, compress every token (retrieval,
+reference mean, SwiGLU residual code, group quantisation), then one decode-style
+sparse read per layer (30% random tokens plus the last 512).  Inputs are resident in
+HBM when the timed region starts; `e2e` repeats the step with the host->device copy
+of the inputs and the device->host copy of the compressed cache inside the timing.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 oracle instead on
+a bounded sample of the same workload, on this host's CPU.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import rkv_workload as wl  # noqa: E402
+
+WORKLOAD = "llama3.1-8b-kv"
+METRIC = "tokens compressed/sec (Llama-3.1-8B KV shape) and % of bf16 tensor roofline"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return (float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]),
+                "measured")
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def workload_description(cfg: wl.Config) -> dict:
+    return {
+        "workload": "%s: %d layers x %d seq x %d tokens, kv width %d (N=%d, D=%d), d_ff=%d, "
+                    "d_c=%d, k=%d, stride %d, INT%d, %s kv/%s refs; step = pool + compress of "
+                    "all layers + one sparse read per layer (30%% random + last %d)" % (
+                        cfg.name, cfg.L, cfg.B, cfg.T, cfg.W, cfg.N, cfg.D, cfg.d_ff, cfg.d_c,
+                        cfg.k, cfg.stride, cfg.bits, cfg.kv_dtype, cfg.ref_dtype, cfg.gather_tail),
+        "layers": cfg.L, "seqs": cfg.B, "tokens": cfg.T, "kv_width": cfg.W, "d_ff": cfg.d_ff,
+        "d_c": cfg.d_c, "bits": cfg.bits, "stride": cfg.stride,
+        "l2": "inputs (%.2f GB kv) exceed the 129 MB L2; no flush" % (
+            cfg.L * cfg.B * cfg.T * cfg.W * 2 / 1e9),
+        "parallelism": "replicas (one independent workload per GPU)",
+    }
+
+
+def algorithmic(cfg: wl.Config):
+    """Algorithmic work of one step (per layer-sequence x L*B): the flops the method
+    needs (distances over the causal pool, the first compressor layer once per token
+    and once per reference, W_c3 once per token) and the read's bytes."""
+    T, s, W, F, C = cfg.T, cfg.stride, cfg.W, cfg.d_ff, cfg.d_c
+    ref_pos = np.arange(cfg.first, T, s)
+    n_ref = ref_pos.size
+    n_non = T - n_ref
+    t = np.arange(T)
+    pool = np.searchsorted(ref_pos, t, side="left")
+    is_ref = np.zeros(T, bool)
+    is_ref[ref_pos] = True
+    pairs = int(pool[~is_ref].sum())
+    LB = cfg.L * cfg.B
+    fl = {
+        "umma_distance_topk": LB * pairs * 2.0 * W,
+        "umma_swiglu_diff": LB * n_non * 4.0 * W * F,
+        "umma_ref_proj": LB * n_ref * 4.0 * W * F,
+        "umma_z_quant": LB * n_non * 2.0 * F * C,
+    }
+    return fl, n_ref, n_non, pairs
+
+
+def gather_bytes_per_token(cfg, out_bytes=2):
+    return (cfg.d_c * cfg.bits // 8 + (cfg.d_c // 32) * 8 + 16 + 4 + cfg.d_c * out_bytes
+            + cfg.W * out_bytes)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q, "--format=csv,noheader",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                mx.append(float(f[2].split()[0]))
+            except Exception:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _gen_inputs(cfg, threads=16):
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        kv = list(ex.map(lambda l: wl.layer_kv(cfg, l), range(cfg.L)))
+        w = list(ex.map(lambda l: wl.layer_weights(cfg, l), range(cfg.L)))
+    return kv, w
+
+
+def cpu_baseline(cfg, n_tokens=192, layer=0):
+    """The oracle as it stands, single-threaded, on evenly spaced tokens of one layer."""
+    import oracle
+    kv = wl.layer_kv(cfg, layer)[0]
+    w = wl.layer_weights(cfg, layer)
+    toks = np.linspace(1, cfg.T - 1, n_tokens).astype(np.int32)
+    toks = toks[toks % cfg.stride != cfg.first % cfg.stride]
+    kv64 = wl.stored_to_f64(kv, cfg.kv_dtype)
+    ref_pos = oracle.schedule(cfg)
+    refs64, _ = oracle.stored_refs(cfg, kv, ref_pos)
+    w64 = oracle.weights_f64(cfg, w)
+    t0 = time.perf_counter()
+    oracle.compress_tokens(cfg, kv, w64, toks, kv64=kv64, refs64=refs64, ref_pos=ref_pos)
+    dt = time.perf_counter() - t0
+    return {"value": toks.size / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d non-reference tokens evenly spaced over layer %d of %s (T=%d), full write "
+                      "path per token (retrieval over the causal pool, mean, f_c twice, quantise), "
+                      "single-threaded fp64 C; %.1f s" % (toks.size, layer, cfg.name, cfg.T, dt)}
+
+
+def run_reference(args, cfg):
+    rank, ws, _ = _dist_env()
+    if rank != 0:
+        return
+    import oracle
+    kv = wl.layer_kv(cfg, 0)[0]
+    w = wl.layer_weights(cfg, 0)
+    kv64 = wl.stored_to_f64(kv, cfg.kv_dtype)
+    ref_pos = oracle.schedule(cfg)
+    refs64, _ = oracle.stored_refs(cfg, kv, ref_pos)
+    w64 = oracle.weights_f64(cfg, w)
+    per_step = 48
+    rng = np.random.default_rng(0)
+    times = []
+    for step in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(np.nonzero(np.arange(cfg.T) % cfg.stride)[0], per_step, replace=False))
+        t0 = time.perf_counter()
+        oracle.compress_tokens(cfg, kv, w64, toks.astype(np.int32), kv64=kv64, refs64=refs64,
+                               ref_pos=ref_pos)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = per_step * len(times) / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_description(cfg),
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": UNIT,
+                             "sample": "per step %d random non-reference tokens of layer 0, full "
+                                       "write path, single-threaded fp64 C" % per_step},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg):
+    import torch
+    rank, ws, local = _dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from reference_residual_kv_gb300 import build as rkv_build
+    from reference_residual_kv_gb300 import rkv
+    rkv_build.build()
+    rkv.lib()
+
+    kv, w = _gen_inputs(cfg)
+    kv_h = torch.from_numpy(np.stack(kv).view(np.int16)).view(torch.bfloat16).pin_memory()
+    W1_h = torch.from_numpy(np.stack([x[0] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    W2_h = torch.from_numpy(np.stack([x[1] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    W3_h = torch.from_numpy(np.stack([x[2] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    del kv, w
+    kv_d, W1, W2, W3 = (t.to(dev) for t in (kv_h, W1_h, W2_h, W3_h))
+
+    p = rkv.params_from_config(cfg)
+    bufs = rkv.Buffers(p, device=dev)
+    LB = cfg.L * cfg.B
+    sels = np.stack([wl.gather_selection(cfg, l, 0) for l in range(LB)])
+    sel = torch.from_numpy(sels).to(dev)
+    n_sel = sel.shape[1]
+    out_z = torch.empty((LB, n_sel, cfg.d_c), dtype=torch.bfloat16, device=dev)
+    out_m = torch.empty((LB, n_sel, cfg.W), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bufs.build_ref_pool(kv_d, stream)
+        bufs.compress(kv_d, W1, W2, W3, stream)
+        bufs.gather(sel, out_z, out_m, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = bufs.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d (%s)" % (st, rkv.rkv_status_string(st)))
+
+    # ---- timed region: inputs resident in HBM
+    barrier()
+    torch.cuda.synchronize(dev)
+    rkv.rkv_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    prof = rkv.rkv_profile_collect()
+    rkv.rkv_profile_enable(False)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = cfg.L * cfg.B * cfg.T
+    value = tokens_per_step * ws / (ms / 1e3)
+
+    # ---- end to end: host buffers in, compressed cache and reads out
+    e2e = None
+    if not args.no_e2e:
+        res_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for t in (bufs.codes, bufs.hdr, bufs.ref_idx, bufs.ref_vec, bufs.ref_sqnorm, out_z, out_m)]
+        h2d = sum(t.numel() * t.element_size() for t in (kv_h, W1_h, W2_h, W3_h))
+        d2h = sum(t.numel() * t.element_size() for t in res_h)
+        srcs = (bufs.codes, bufs.hdr, bufs.ref_idx, bufs.ref_vec, bufs.ref_sqnorm, out_z, out_m)
+
+        def e2e_step():
+            for d, h in zip((kv_d, W1, W2, W3), (kv_h, W1_h, W2_h, W3_h)):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(res_h, srcs):
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = a.elapsed_time(b) / n_e2e
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": tokens_per_step * ws / (ms_e2e / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": ms_e2e}
+    if rank != 0:
+        return
+
+    hbm, tf_burst, tf_sust, src = _peaks()
+    fl, n_ref, n_non, pairs = algorithmic(cfg)
+    kernels = {}
+    for name, (tot, cnt) in prof.items():
+        ent = {"ms_per_launch": tot / cnt, "launches": cnt, "share": None}
+        if name in fl:
+            ent["tflops"] = fl[name] / (tot / cnt / 1e3) / 1e12
+        kernels[name] = ent
+    tot_all = sum(v[0] for v in prof.values())
+    for name in kernels:
+        kernels[name]["share"] = prof[name][0] / tot_all
+    dom = max((n for n in prof if n in fl), key=lambda n: prof[n][0])
+    dom_ms = prof[dom][0] / prof[dom][1]
+    achieved = fl[dom] / (dom_ms / 1e3) / 1e12
+    f_alg = sum(fl.values())
+    compress_ms = sum(prof[n][0] / args.steps for n in prof if n != "gather_dequant")
+    g_ms = prof.get("gather_dequant", (float("nan"), 1))
+    g_bytes = LB * n_sel * gather_bytes_per_token(cfg) + LB * n_ref * cfg.W * 2
+    g_gbs = g_bytes / (g_ms[0] / g_ms[1] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+        "config": workload_description(cfg),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tf_sust,
+                     "unit": "TFLOP/s", "frac": achieved / tf_sust, "traffic": None,
+                     "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % src,
+                     "algorithmic_flops_per_launch": fl[dom]},
+        "compress_roofline": {"flops_per_step": f_alg, "ms_per_step": compress_ms,
+                              "achieved_tflops": f_alg / (compress_ms / 1e3) / 1e12,
+                              "frac_of_sustained": f_alg / (compress_ms / 1e3) / 1e12 / tf_sust,
+                              "frac_of_burst": f_alg / (compress_ms / 1e3) / 1e12 / tf_burst},
+        "gather_roofline": {"bound": "hbm", "tokens_per_launch": LB * n_sel,
+                            "bytes_per_launch": g_bytes, "achieved": g_gbs, "peak": hbm,
+                            "unit": "GB/s", "frac": g_gbs / hbm,
+                            "gathered_tokens_per_s": LB * n_sel / (g_ms[0] / g_ms[1] / 1e3)},
+        "kernels": kernels,
+        "gpu_launches": int(sum(v[1] for v in prof.values())),
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws >= 1:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=WORKLOAD, choices=list(wl.CONFIGS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = wl.CONFIGS[args.config]
+    if cfg.gather_steps == 0:
+        cfg = cfg.replace(gather_steps=1)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

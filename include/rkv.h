@@ -1,0 +1,168 @@
+/*
+ * rkv.h -- C ABI of librkv: the ResidualKV cache-write path and its sparse read
+ * path on one GB300 GPU (sm_103a).
+ *
+ * Citations name sections of the reading-notes page "ResidualKV：基于参考向量与
+ * 残差的 KV Cache 压缩" (on "ResidualKV: Residual-Based KV Cache Compression for
+ * Efficient Long-Context Inference", arXiv 2602.08005v2), written [RKV §x = paper y].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array arguments are DEVICE pointers owned by the caller (for instance
+ *   torch allocations); the library keeps no pointer after a call returns and
+ *   allocates no device memory of its own.  Scratch comes from a caller-provided
+ *   workspace whose size rkv_query_sizes() reports.
+ * - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *   default stream) and runs asynchronously; outputs are valid once the stream
+ *   has been synchronised.
+ * - Every device buffer must start on a 16-byte boundary.
+ * - Host-side validation runs before anything is enqueued: on an error nothing is
+ *   launched and the function returns the error.  A launch failure returns
+ *   RKV_ERR_CUDA.  Errors found on the device (an out-of-range index, a wait
+ *   that timed out) are written to *dev_status (an int32 in device memory that
+ *   the caller sets to RKV_OK before the call; the first error wins) and the
+ *   kernel skips the offending work instead of faulting.  Nothing traps, exits
+ *   or prints.
+ *
+ * Shapes (per rkv_params):  L layers, B sequences per layer, T tokens per
+ * sequence, W = 2*N*D (K of all heads concatenated with V of all heads, pre-RoPE,
+ * [RKV §2.1 = Sec. IV-A]), n_ref references per sequence (rkv_n_ref()).
+ * Per-(layer, sequence) arrays are stacked with the layer index outermost:
+ * index lb = layer*B + b.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rkv_status {
+    RKV_OK = 0,
+    RKV_ERR_INVALID_ARG = 1,     /* null pointer, bad size or inconsistent params   */
+    RKV_ERR_UNSUPPORTED = 2,     /* valid for the method, not handled by this build */
+    RKV_ERR_ALIGNMENT = 3,       /* a buffer is not 16-byte aligned                  */
+    RKV_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed             */
+    RKV_ERR_INDEX = 5,           /* device-detected: index out of range              */
+    RKV_ERR_DEVICE_TIMEOUT = 6,  /* device-detected: a bounded wait expired          */
+    RKV_ERR_WORKSPACE = 7        /* workspace smaller than rkv_query_sizes() asks    */
+} rkv_status;
+
+typedef enum rkv_dtype {
+    RKV_F32 = 0,
+    RKV_BF16 = 1,
+    RKV_FP8_E4M3 = 2             /* OCP OFP8 E4M3: round to nearest even, saturating */
+} rkv_dtype;
+
+typedef struct rkv_params {
+    int32_t L;          /* layers; each has its own compressor weights               */
+    int32_t B;          /* sequences per layer (same T, same reference schedule)     */
+    int32_t T;          /* tokens per sequence, >= 1                                  */
+    int32_t N, D;       /* KV heads and head dim: W = 2*N*D, W % 8 == 0               */
+    int32_t d_ff;       /* compressor hidden width   [RKV §2.3 = Sec. IV-A]           */
+    int32_t d_c;        /* latent code width, d_c % group == 0                        */
+    int32_t k;          /* references per token, 1..4 (paper default 4) [RKV §2.2]    */
+    int32_t group;      /* quantisation group, 32 [RKV §2.4]                          */
+    int32_t bits;       /* 2 or 4 [RKV §2.4]                                          */
+    int32_t kv_dtype;   /* RKV_F32 or RKV_BF16: kv and compressor weights             */
+    int32_t ref_dtype;  /* kv_dtype, or RKV_FP8_E4M3 (bf16 kv only) [RKV §2.4 = V-A]  */
+    int32_t stride;     /* fixed reference stride s >= 1 [RKV §2.6 = Sec. IV-A]       */
+    int32_t first;      /* position of the first reference, 0 <= first               */
+} rkv_params;
+
+/* Reference pool [RKV §2.2, §2.6 = Sec. IV-A]; filled by rkv_build_ref_pool.
+ * References are stored uncompressed (or FP8) and are the values every later
+ * step uses (encoder and decoder share them [RKV §2.5 = Sec. IV-B]).            */
+typedef struct rkv_ref_pool {
+    int32_t *ref_pos;     /* [n_ref]  position of reference slot m, ascending       */
+    int32_t *ref_slot;    /* [T]      slot of token t if it is a reference, else -1 */
+    int32_t *pool_size;   /* [T]      number of references at positions < t         */
+    void    *ref_vec;     /* [L*B][n_ref][W] in ref_dtype                            */
+    float   *ref_sqnorm;  /* [L*B][n_ref] squared L2 norm of the stored reference   */
+} rkv_ref_pool;
+
+/* Compressed per-token records [RKV §2.4]: each token owns its codes, its group
+ * extremes and its reference relation, so one token can be read alone.
+ *  codes:   [L*B][T][d_c*bits/8] bytes; INT4: coordinate 2j in the low nibble of
+ *           byte j, 2j+1 in the high nibble; INT2: coordinate 4j+i in bits 2i..2i+1.
+ *  hdr:     [L*B][T][d_c/group][2] float {z_min, delta}; z~ = q*delta + z_min.
+ *  ref_idx: [L*B][T][4] int32 reference slots, ascending, -1 padded (k_t = number
+ *           of entries >= 0).  A reference token stores {own slot,-1,-1,-1}, zero
+ *           codes and zero extremes, so that a read returns the reference itself. */
+typedef struct rkv_cache {
+    uint8_t *codes;
+    float   *hdr;
+    int32_t *ref_idx;
+} rkv_cache;
+
+/* Number of references per sequence for the fixed schedule: positions first,
+ * first+stride, ... < T.  Returns -1 on invalid params.                          */
+int32_t rkv_n_ref(const rkv_params *p);
+
+/* Host-only: bytes the caller must provide.  Any output pointer may be NULL.
+ *  pool_bytes:      ref_vec + ref_sqnorm + the three int32 schedule arrays
+ *  cache_bytes:     codes + hdr + ref_idx
+ *  workspace_bytes: scratch for rkv_compress                                     */
+rkv_status rkv_query_sizes(const rkv_params *p, size_t *pool_bytes, size_t *cache_bytes,
+                           size_t *workspace_bytes);
+
+/* Step 0 of the write path: the fixed-stride schedule [RKV §2.6 = Sec. IV-A] and
+ * the stored references.  kv: [L*B][T][W] in kv_dtype.  Writes every field of
+ * *pool; with ref_dtype = RKV_FP8_E4M3 each reference is rounded to E4M3
+ * (nearest even, saturating) and ref_sqnorm is taken over the rounded values.    */
+rkv_status rkv_build_ref_pool(const rkv_params *p, const void *kv, const rkv_ref_pool *pool,
+                              void *stream);
+
+/* The write path [RKV §2.2-§2.4 = Sec. IV-A] for every token of every (layer,
+ * sequence), given the pool from rkv_build_ref_pool:
+ *  1. retrieval: for a non-reference token t, the k_t = min(k, pool_size[t])
+ *     references with pos < t nearest in squared L2 (ties -> lower slot);
+ *  2. mean of those references in KV space;
+ *  3. z_t = f_c(kv_t) - f_c(mean_t),  f_c(x) = (Swish(x W_c1) ⊙ x W_c2) W_c3;
+ *  4. per-token groups of `group` coordinates quantised with min/max scaling to
+ *     `bits` bits (a constant group is stored exactly: delta = 0).
+ * Weights are stored out-major, one set per layer, in kv_dtype:
+ *  W1t, W2t: [L][d_ff][W] with W1t[f][c] = W_c1[c][f];  W3t: [L][d_c][d_ff].
+ * workspace: >= workspace_bytes from rkv_query_sizes, 256-byte aligned.
+ * z_out (nullable): [L*B][T][d_c] fp32 unquantised z (0 for reference tokens).
+ * dev_status: device int32, set to RKV_OK by the caller.                         */
+rkv_status rkv_compress(const rkv_params *p, const void *kv, const rkv_ref_pool *pool,
+                        const void *W1t, const void *W2t, const void *W3t,
+                        const rkv_cache *cache, void *workspace, size_t workspace_bytes,
+                        float *z_out, int32_t *dev_status, void *stream);
+
+/* The sparse read [RKV §2.7 = Sec. IV-C]: for each selected token read only its
+ * own record and its references, and return
+ *   out_z[lb][i]    = dequantised z~ of token sel[lb][i]        ([L*B][n_sel][d_c])
+ *   out_mean[lb][i] = mean of its stored references in KV space ([L*B][n_sel][W])
+ * in out_dtype (RKV_F32 or RKV_BF16; fp32 arithmetic, one rounding at the end).
+ * sel: [L*B][n_sel] int32 token positions; an entry of -1 is padding and yields
+ * zero rows; an entry >= T sets RKV_ERR_INDEX and yields zero rows.  Unselected
+ * tokens' records are never read.  With n_sel = T and sel = 0..T-1 this is the
+ * paper's standalone mode (every code restored).                                 */
+rkv_status rkv_gather_dequant(const rkv_params *p, const rkv_ref_pool *pool,
+                              const rkv_cache *cache, const int32_t *sel, int32_t n_sel,
+                              void *out_z, void *out_mean, int32_t out_dtype,
+                              int32_t *dev_status, void *stream);
+
+/* Diagnostics: per-kernel device time.  rkv_profile_enable(1) clears the record
+ * and brackets every later kernel launch of the library with two CUDA events on
+ * the launch stream; rkv_profile_enable(0) stops recording.  rkv_profile_collect
+ * waits for the recorded events and writes, per kernel name, the summed elapsed
+ * milliseconds and the launch count: names is a caller buffer of max_entries rows
+ * of name_len chars.  Returns the number of rows written, or -1 on error.  Not
+ * thread-safe; meant for benchmarks.                                             */
+rkv_status rkv_profile_enable(int32_t on);
+int32_t rkv_profile_collect(char *names, int32_t name_len, float *total_ms, int32_t *launches,
+                            int32_t max_entries);
+
+/* Static description of a status code. */
+const char *rkv_status_string(rkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H */

@@ -72,6 +72,9 @@ def lib():
             [ctypes.c_int] * 7 + [_dp, _dp, _ip, ctypes.c_int, _dp, _dp, _dp, _ip, ctypes.c_int, _ip,
                                   _ip, _ip, _dp, _dp, _up, _dp, _dp, _dp])
         L.rkvo_compress_tokens.restype = None
+        L.rkvo_retrieve_tokens.argtypes = ([ctypes.c_int] * 2 + [_dp, _dp, _ip, ctypes.c_int, _ip,
+                                                                ctypes.c_int, _ip, _ip, _dp])
+        L.rkvo_retrieve_tokens.restype = None
         L.rkvo_gather.argtypes = ([ctypes.c_int] * 4 + [_dp, _up, _dp, _dp, _ip, _ip, ctypes.c_int, _dp, _dp])
         L.rkvo_gather.restype = None
     return _lib
@@ -259,3 +262,25 @@ def gather(cfg: wl.Config, refs64, q, zmin, delta, idx, sel):
     lib().rkvo_gather(cfg.W, cfg.d_c, cfg.group, cfg.k, prf, pq, pmn, pdl, pidx, psel, n,
                       zq.ctypes.data_as(_dp), mn.ctypes.data_as(_dp))
     return zq, mn
+
+
+def retrieve_tokens(cfg: wl.Config, kv_seq, tokens, kv64=None, refs64=None, ref_pos=None):
+    """Reference sets of `tokens` of one (layer, sequence): (idx [n][k], k_i [n], dk [n][2])."""
+    if ref_pos is None:
+        ref_pos = schedule(cfg)
+    if kv64 is None:
+        kv64 = wl.stored_to_f64(kv_seq, cfg.kv_dtype)
+    if refs64 is None:
+        refs64, _ = stored_refs(cfg, kv_seq, ref_pos)
+    tokens = np.asarray(tokens, dtype=np.int32)
+    n = tokens.size
+    kv64, pkv = _d(kv64)
+    refs64, prf = _d(refs64 if refs64.size else np.zeros((1, cfg.W)))
+    ref_pos, ppos = _i(ref_pos)
+    tokens, ptok = _i(tokens)
+    idx = np.zeros((n, cfg.k), np.int32)
+    ki = np.zeros(n, np.int32)
+    dk = np.zeros((n, 2))
+    lib().rkvo_retrieve_tokens(cfg.W, cfg.k, pkv, prf, ppos, ref_pos.size, ptok, n,
+                               idx.ctypes.data_as(_ip), ki.ctypes.data_as(_ip), dk.ctypes.data_as(_dp))
+    return idx, ki, dk

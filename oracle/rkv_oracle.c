@@ -346,3 +346,28 @@ void rkvo_gather(int W, int d_c, int group, int k, const double *refs,
         rkvo_mean(refs, ix, ki, W, mean_out + (size_t)n * W);
     }
 }
+
+/* Retrieval alone (§2.2) for a list of tokens of one sequence: idx [n_tok][k]
+ * (reference tokens get {own slot, -1, ...}), k_i [n_tok], dk [n_tok][2].        */
+void rkvo_retrieve_tokens(int W, int k, const double *kv, const double *refs,
+                          const int32_t *ref_pos, int n_ref, const int32_t *tokens, int n_tok,
+                          int32_t *idx, int32_t *ki_out, double *dk)
+{
+    for (int n = 0; n < n_tok; n++) {
+        int t = tokens[n], own = -1, n_pool = 0;
+        for (int m = 0; m < n_ref; m++) {
+            if (ref_pos[m] == t) own = m;
+            if (ref_pos[m] < t) n_pool++;
+        }
+        int32_t *ix = idx + (size_t)n * k;
+        if (own >= 0) {
+            ix[0] = own;
+            for (int m = 1; m < k; m++) ix[m] = -1;
+            ki_out[n] = 1;
+            dk[2 * n] = 0.0;
+            dk[2 * n + 1] = INFINITY;
+            continue;
+        }
+        ki_out[n] = rkvo_retrieve(kv + (size_t)t * W, refs, n_pool, W, k, ix, dk + 2 * n);
+    }
+}

@@ -1,0 +1,163 @@
+// rkv_gather.cu -- the sparse read [RKV §2.7 = Sec. IV-C]: a sparse-attention step
+// names the tokens it needs; for each, read only that token's record (codes, group
+// extremes, reference slots) and its stored references, and return the dequantised
+// code z~ = q*delta + z_min [RKV §2.4] and the reference mean in KV space [RKV §2.2].
+// Groups never span tokens [RKV §2.4], so no unselected neighbour is touched.
+//
+// One warp per selected token.  Records are read with 8/16-byte loads, references
+// with 16-byte loads (L2-resident: one sequence's pool is a few MB), outputs are
+// written with 16-byte stores.
+#include "rkv_internal.cuh"
+
+namespace rkv {
+
+template <typename T> struct RefLoad;
+template <> struct RefLoad<float> {       // 8 consecutive fp32 values
+    static __device__ __forceinline__ void add(const float *p, float (&a)[8])
+    {
+        float4 u = *(const float4 *)p, v = *(const float4 *)(p + 4);
+        a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+        a[4] += v.x; a[5] += v.y; a[6] += v.z; a[7] += v.w;
+    }
+};
+template <> struct RefLoad<__nv_bfloat16> {
+    static __device__ __forceinline__ void add(const __nv_bfloat16 *p, float (&a)[8])
+    {
+        uint4 raw = *(const uint4 *)p;
+        const __nv_bfloat16 *h = (const __nv_bfloat16 *)&raw;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] += __bfloat162float(h[j]);
+    }
+};
+template <> struct RefLoad<uint8_t> {     // FP8 E4M3
+    static __device__ __forceinline__ void add(const uint8_t *p, float (&a)[8])
+    {
+        uint2 raw = *(const uint2 *)p;
+        const uint8_t *b = (const uint8_t *)&raw;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __nv_fp8_e4m3 q;
+            q.__x = b[j];
+            a[j] += (float)q;
+        }
+    }
+};
+
+template <typename OutT>
+__device__ __forceinline__ void store8(OutT *dst, const float (&v)[8]);
+template <> __device__ __forceinline__ void store8<float>(float *dst, const float (&v)[8])
+{
+    *(float4 *)dst = make_float4(v[0], v[1], v[2], v[3]);
+    *(float4 *)(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&v)[8])
+{
+    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
+    *(uint4 *)dst = *(const uint4 *)o;
+}
+
+template <typename RefT, typename OutT>
+__global__ void __launch_bounds__(256)
+k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int bits,
+         int n_ref, const RefT *__restrict__ ref_vec, const uint8_t *__restrict__ codes,
+         const float2 *__restrict__ hdr, const int4 *__restrict__ ref_idx, OutT *__restrict__ out_z,
+         OutT *__restrict__ out_mean, long long total, int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= total) return;
+    const int lb = (int)(gw / n_sel);
+    const int t = __ldg(sel + gw);
+    OutT *oz = out_z + (size_t)gw * d_c;
+    OutT *om = out_mean + (size_t)gw * W;
+    const float zero8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+
+    bool ok = t >= 0 && t < T;
+    if (t >= T) set_status(status, RKV_ERR_INDEX);
+    int slots[4] = {-1, -1, -1, -1};
+    int k = 0;
+    const size_t rec = (size_t)lb * T + (ok ? t : 0);
+    if (ok) {
+        int4 ix = __ldg(ref_idx + rec);
+        slots[0] = ix.x; slots[1] = ix.y; slots[2] = ix.z; slots[3] = ix.w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (slots[j] >= n_ref) { ok = false; set_status(status, RKV_ERR_INDEX); }
+            if (slots[j] >= 0) ++k;
+        }
+    }
+    if (!ok) {
+        for (int c = lane * 8; c < d_c; c += 256) store8(oz + c, zero8);
+        for (int c = lane * 8; c < W; c += 256) store8(om + c, zero8);
+        return;
+    }
+
+    // z~: each lane decodes 8 coordinates per step
+    const int pitch = d_c * bits / 8;
+    const uint8_t *crow = codes + rec * pitch;
+    const float2 *hrow = hdr + rec * (d_c / 32);
+    for (int c = lane * 8; c < d_c; c += 256) {
+        float2 h = __ldg(hrow + (c >> 5));
+        uint32_t word;
+        if (bits == 4) word = __ldg((const uint32_t *)(crow + (c >> 1)));
+        else word = (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t q = bits == 4 ? (word >> (4 * j)) & 15u : (word >> (2 * j)) & 3u;
+            v[j] = fmaf((float)q, h.y, h.x);
+        }
+        store8(oz + c, v);
+    }
+
+    // mean of the stored references, summed in ascending slot order, then / k
+    const RefT *rbase = ref_vec + (size_t)lb * n_ref * W;
+    for (int c = lane * 8; c < W; c += 256) {
+        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a);
+        const float fk = (float)k;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = k > 0 ? __fdiv_rn(a[j], fk) : 0.0f;
+        store8(om + c, a);
+    }
+}
+
+template <typename RefT>
+static void gather_out(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
+                       const int32_t *sel, int n_sel, void *out_z, void *out_mean, int out_dtype,
+                       int32_t *status, cudaStream_t s)
+{
+    long long total = (long long)g.LB * n_sel;
+    unsigned blocks = (unsigned)((total * 32 + 255) / 256);
+    ProfScope prof("gather_dequant", s);
+    if (out_dtype == RKV_BF16)
+        k_gather<RefT, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+            sel, n_sel, g.T, g.W, g.d_c, g.bits, g.n_ref, (const RefT *)pool->ref_vec, cache->codes,
+            (const float2 *)cache->hdr, (const int4 *)cache->ref_idx, (__nv_bfloat16 *)out_z,
+            (__nv_bfloat16 *)out_mean, total, status);
+    else
+        k_gather<RefT, float><<<blocks, 256, 0, s>>>(
+            sel, n_sel, g.T, g.W, g.d_c, g.bits, g.n_ref, (const RefT *)pool->ref_vec, cache->codes,
+            (const float2 *)cache->hdr, (const int4 *)cache->ref_idx, (float *)out_z,
+            (float *)out_mean, total, status);
+}
+
+cudaError_t launch_gather(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
+                          const int32_t *sel, int n_sel, void *out_z, void *out_mean,
+                          int out_dtype, int32_t *status, cudaStream_t s)
+{
+    if (g.ref_dtype == RKV_F32)
+        gather_out<float>(g, pool, cache, sel, n_sel, out_z, out_mean, out_dtype, status, s);
+    else if (g.ref_dtype == RKV_BF16)
+        gather_out<__nv_bfloat16>(g, pool, cache, sel, n_sel, out_z, out_mean, out_dtype, status, s);
+    else
+        gather_out<uint8_t>(g, pool, cache, sel, n_sel, out_z, out_mean, out_dtype, status, s);
+    return cudaGetLastError();
+}
+
+}  // namespace rkv

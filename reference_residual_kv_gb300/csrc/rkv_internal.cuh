@@ -1,0 +1,152 @@
+// rkv_internal.cuh -- declarations shared by the librkv translation units.
+//
+// Citations: [RKV §x = paper y] names a section of the reading-notes page
+// "ResidualKV：基于参考向量与残差的 KV Cache 压缩" (arXiv 2602.08005v2) and the
+// paper section it summarises.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/rkv.h"
+
+namespace rkv {
+
+// Retrieval: number of expansion candidates kept per token and chunk, and the
+// relative error budget of the tensor-core distance expansion.  A token's top-k
+// is accepted from the expansion only if its k-th/(k+1)-th gap exceeds twice
+// kTau * (max ||r||^2 + 2 ||x|| max ||r||); otherwise it is re-ranked with exact
+// differences.
+constexpr int kCand = 8;
+constexpr float kTau = 1.0f / 32768.0f;   // 2^-15
+constexpr int kMaxK = 4;                  // ref_idx rows are int4
+
+// tcgen05 GEMM tiling: 128 token rows x 256 columns, K chunks of 64 bf16.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kDistChunk = 8;             // N-tiles (2048 references) per distance work item
+
+// Bounded waits: ~1 s at 2 GHz.
+constexpr long long kWaitCycles = 2000000000LL;
+
+struct Geometry {
+    int L, B, LB, T, W, d_ff, d_c, k, bits, n_ref, n_groups, code_pitch;
+    int kv_dtype, ref_dtype;
+    int stride, first;
+    int n_mtiles;        // ceil(T / 128)
+    int max_chunks;      // distance work items per token tile
+};
+
+Geometry make_geometry(const rkv_params *p);
+
+// Workspace carve-up (offsets in bytes from the workspace base, 256-aligned).
+struct Workspace {
+    size_t ref_mma;      // bf16 [LB][n_ref][W]   decoded FP8 references (FP8 only)
+    size_t P1, P2;       // f32  [LB][n_ref][d_ff]
+    size_t rn_max;       // f32  [LB]
+    size_t cand;         // f32x2 [LB][T][max_chunks][kCand]  (tensor-core path)
+    size_t dh_hi, dh_lo; // bf16 [LB][T][d_ff]   (tensor-core path)
+    size_t dh32;         // f32  [LB][T][d_ff]   (fp32 path)
+    size_t z32;          // f32  [LB][T][d_c]    (fp32 path)
+    size_t total;
+};
+Workspace workspace_layout(const Geometry &g);
+
+// ---- launchers (each returns cudaGetLastError()) ----------------------------
+cudaError_t launch_build_schedule(const Geometry &g, const rkv_ref_pool *pool, cudaStream_t s);
+cudaError_t launch_build_refs(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
+                              cudaStream_t s);
+cudaError_t launch_prep_refs(const Geometry &g, const rkv_ref_pool *pool, void *ref_mma,
+                             float *rn_max, cudaStream_t s);
+cudaError_t launch_gather(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
+                          const int32_t *sel, int n_sel, void *out_z, void *out_mean,
+                          int out_dtype, int32_t *status, cudaStream_t s);
+
+// fp32 path (CUDA cores): projections, top-k by exact distances, z, quantisation
+cudaError_t launch_simt_compress(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
+                                 const void *W1t, const void *W2t, const void *W3t,
+                                 const rkv_cache *cache, uint8_t *ws, const Workspace &wl,
+                                 float *z_out, int32_t *status, cudaStream_t s);
+
+// bf16 path (tcgen05 + TMA)
+cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
+                                 const void *W1t, const void *W2t, const void *W3t,
+                                 const rkv_cache *cache, uint8_t *ws, const Workspace &wl,
+                                 float *z_out, int32_t *status, cudaStream_t s);
+
+// top-k finalisation shared by both paths: exact re-rank / full scan
+cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
+                                 int ref_exact_is_f32, const rkv_ref_pool *pool,
+                                 const float2 *cand, const float *rn_max, int32_t *ref_idx,
+                                 int32_t *status, cudaStream_t s);
+
+int device_sm_count();
+
+// per-kernel event timing (rkv_prof.cu); no-ops unless rkv_profile_enable(1)
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+struct ProfScope {
+    cudaStream_t s;
+    ProfScope(const char *name, cudaStream_t st) : s(st) { prof_begin(name, st); }
+    ~ProfScope() { prof_end(s); }
+};
+
+// ---- device helpers ---------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t *st, int code)
+{
+    if (st) atomicCAS(st, 0, code);
+}
+
+// Number of N-tiles (256 references) a 128-token tile needs: its last row's pool.
+__device__ __forceinline__ int dist_ntiles(const int32_t *pool_size, int T, int m)
+{
+    int last = min(T, (m + 1) * kBM) - 1;
+    int pool = pool_size[last];
+    return (pool + kBN - 1) / kBN;
+}
+
+__device__ __forceinline__ float silu(float u)
+{
+    return u / (1.0f + __expf(-u));
+}
+
+// [RKV §2.4 = Sec. IV-A] min/max quantisation of one group of 32 latent values.
+// delta = (max - min)/(2^b - 1) (IEEE division), q = floor((z - min)/delta + 1/2)
+// clamped to [0, 2^b - 1]; max == min stores the constant with delta = 0, q = 0.
+// Packs INT4 as 4 words (coordinate 2j low nibble of byte j) and INT2 as 2 words
+// (coordinate 4j+i in bits 2i..2i+1 of byte j).
+__device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, uint32_t (&w)[4],
+                                              float &zmin, float &delta)
+{
+    float lo = v[0], hi = v[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+        lo = fminf(lo, v[j]);
+        hi = fmaxf(hi, v[j]);
+    }
+    const int qmax = (1 << bits) - 1;
+    zmin = lo;
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    if (hi == lo) {
+        delta = 0.0f;
+        return;
+    }
+    const float dl = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
+    delta = dl;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float u = __fadd_rn(__fdiv_rn(__fsub_rn(v[j], lo), dl), 0.5f);
+        int q = (int)floorf(u);
+        q = q < 0 ? 0 : (q > qmax ? qmax : q);
+        if (bits == 4)
+            w[j >> 3] |= (uint32_t)q << (4 * (j & 7));
+        else
+            w[j >> 4] |= (uint32_t)q << (2 * (j & 15));
+    }
+}
+
+}  // namespace rkv

@@ -1,0 +1,168 @@
+// rkv_pool.cu -- reference schedule and stored references
+// [RKV §2.6 = Sec. IV-A fixed stride; §2.4 / §2.5 = Sec. IV-A, IV-B, V-A: references
+// are kept uncompressed or as FP8, and every later step uses the stored values].
+#include "rkv_internal.cuh"
+
+namespace rkv {
+
+// ref_slot[t], pool_size[t] for t < T and ref_pos[m] for m < n_ref.
+__global__ void k_schedule(int T, int stride, int first, int n_ref, int32_t *ref_pos,
+                           int32_t *ref_slot, int32_t *pool_size)
+{
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < T) {
+        int rel = t - first;
+        ref_slot[t] = (rel >= 0 && rel % stride == 0) ? rel / stride : -1;
+        // references at first + m*stride < t
+        pool_size[t] = rel <= 0 ? 0 : (rel + stride - 1) / stride;
+    }
+    if (t < n_ref) ref_pos[t] = first + t * stride;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One warp per (lb, reference slot): copy (or FP8-encode) the token's row and take
+// the squared norm of the stored values in fp32.
+template <typename TIn, int OUT_FP8>
+__global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restrict__ ref_pos,
+                             void *ref_vec, float *__restrict__ ref_sqnorm, int LB, int T, int W,
+                             int n_ref)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= (long long)LB * n_ref) return;
+    const int lb = (int)(gw / n_ref), m = (int)(gw % n_ref);
+    const TIn *src = kv + ((size_t)lb * T + ref_pos[m]) * W;
+    float acc = 0.0f;
+    if constexpr (sizeof(TIn) == 4) {
+        float *dst = (float *)ref_vec + ((size_t)lb * n_ref + m) * W;
+        for (int c = lane * 4; c < W; c += 128) {
+            float4 v = *(const float4 *)(src + c);
+            *(float4 *)(dst + c) = v;
+            acc += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+    } else {
+        for (int c = lane * 8; c < W; c += 256) {
+            uint4 raw = *(const uint4 *)(src + c);
+            const __nv_bfloat16 *h = (const __nv_bfloat16 *)&raw;
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(h[j]);
+            if constexpr (OUT_FP8) {
+                uint8_t b[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    b[j] = (uint8_t)__nv_cvt_float_to_fp8(f[j], __NV_SATFINITE, __NV_E4M3);
+                    __nv_fp8_e4m3 q;
+                    q.__x = b[j];
+                    f[j] = (float)q;
+                }
+                uint8_t *dst = (uint8_t *)ref_vec + ((size_t)lb * n_ref + m) * W;
+                *(uint2 *)(dst + c) = *(const uint2 *)b;
+            } else {
+                __nv_bfloat16 *dst = (__nv_bfloat16 *)ref_vec + ((size_t)lb * n_ref + m) * W;
+                *(uint4 *)(dst + c) = raw;
+            }
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += f[j] * f[j];
+            acc += s;
+        }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) ref_sqnorm[(size_t)lb * n_ref + m] = acc;
+}
+
+cudaError_t launch_build_schedule(const Geometry &g, const rkv_ref_pool *pool, cudaStream_t s)
+{
+    int n = g.T > g.n_ref ? g.T : g.n_ref;
+    ProfScope prof("build_schedule", s);
+    k_schedule<<<(n + 255) / 256, 256, 0, s>>>(g.T, g.stride, g.first, g.n_ref, pool->ref_pos,
+                                               pool->ref_slot, pool->pool_size);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_refs(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
+                              cudaStream_t s)
+{
+    long long warps = (long long)g.LB * g.n_ref;
+    unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+    ProfScope prof("build_refs", s);
+    if (g.kv_dtype == RKV_F32)
+        k_build_refs<float, 0><<<blocks, 256, 0, s>>>((const float *)kv, pool->ref_pos,
+                                                      pool->ref_vec, pool->ref_sqnorm, g.LB, g.T,
+                                                      g.W, g.n_ref);
+    else if (g.ref_dtype == RKV_FP8_E4M3)
+        k_build_refs<__nv_bfloat16, 1><<<blocks, 256, 0, s>>>(
+            (const __nv_bfloat16 *)kv, pool->ref_pos, pool->ref_vec, pool->ref_sqnorm, g.LB, g.T,
+            g.W, g.n_ref);
+    else
+        k_build_refs<__nv_bfloat16, 0><<<blocks, 256, 0, s>>>(
+            (const __nv_bfloat16 *)kv, pool->ref_pos, pool->ref_vec, pool->ref_sqnorm, g.LB, g.T,
+            g.W, g.n_ref);
+    return cudaGetLastError();
+}
+
+// ---- compress-time preparation -------------------------------------------------
+// FP8 references decoded to bf16 (exact: every E4M3 value is a bf16 value) so that
+// the tensor cores can read them next to bf16 tokens.
+__global__ void k_decode_fp8_refs(const uint8_t *__restrict__ src, __nv_bfloat16 *__restrict__ dst,
+                                  long long n8)
+{
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (long long)gridDim.x * blockDim.x) {
+        uint2 raw = ((const uint2 *)src)[i];
+        const uint8_t *b = (const uint8_t *)&raw;
+        __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __nv_fp8_e4m3 q;
+            q.__x = b[j];
+            o[j] = __float2bfloat16_rn((float)q);
+        }
+        ((uint4 *)dst)[i] = *(const uint4 *)o;
+    }
+}
+
+// rn_max[lb] = max_m ref_sqnorm[lb][m]  (scale of the distance-expansion error bound)
+__global__ void k_rn_max(const float *__restrict__ rn, float *__restrict__ out, int n_ref)
+{
+    __shared__ float sm[32];
+    const int lb = blockIdx.x;
+    float v = 0.0f;
+    for (int m = threadIdx.x; m < n_ref; m += blockDim.x) v = fmaxf(v, rn[(size_t)lb * n_ref + m]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        v = threadIdx.x < (blockDim.x >> 5) ? sm[threadIdx.x] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (threadIdx.x == 0) out[lb] = v;
+    }
+}
+
+cudaError_t launch_prep_refs(const Geometry &g, const rkv_ref_pool *pool, void *ref_mma,
+                             float *rn_max, cudaStream_t s)
+{
+    if (g.n_ref == 0) return cudaMemsetAsync(rn_max, 0, sizeof(float) * g.LB, s);
+    if (g.ref_dtype == RKV_FP8_E4M3) {
+        long long n8 = (long long)g.LB * g.n_ref * g.W / 8;
+        int blocks = (int)((n8 + 255) / 256);
+        if (blocks > 4 * 1024) blocks = 4 * 1024;
+        ProfScope prof("decode_fp8_refs", s);
+        k_decode_fp8_refs<<<blocks, 256, 0, s>>>((const uint8_t *)pool->ref_vec,
+                                                 (__nv_bfloat16 *)ref_mma, n8);
+    }
+    ProfScope prof("ref_norm_max", s);
+    k_rn_max<<<g.LB, 256, 0, s>>>(pool->ref_sqnorm, rn_max, g.n_ref);
+    return cudaGetLastError();
+}
+
+}  // namespace rkv

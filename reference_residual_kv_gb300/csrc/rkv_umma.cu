@@ -1,0 +1,529 @@
+// rkv_umma.cu -- the write path for bf16 kv on the 5th-generation tensor cores.
+//
+// All four dense contractions of the path run through one persistent,
+// warp-specialised kernel (one CTA per SM):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 4 stages
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, bf16 -> fp32,
+//               into one of two 256-column TMEM accumulators
+//   warps 2..5  epilogue: one accumulator row (= one token or reference) per
+//               thread, read with tcgen05.ld while the next tile accumulates
+// The epilogue is what differs between the four uses:
+//   M_P    P1 | P2 = R [W_c1 | W_c2] for each stored reference (fp32 out)
+//   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kCand per row
+//          [RKV §2.2 = Sec. IV-A; ||x||^2 is common to a row and left out]
+//   M_S1   dh = Swish(x W_c1) ⊙ x W_c2 - Swish(p1) ⊙ p2, p = mean of the chosen
+//          references' P rows, i.e. the first layer of f_c at the KV-space mean
+//          by linearity [RKV §2.2, §2.3 = Sec. IV-A]; stored as bf16 hi + lo
+//   M_S2   z = dh_hi W_c3 + dh_lo W_c3 = f_c(kv) - f_c(mean), then per-token
+//          group min/max quantisation and packing [RKV §2.4]
+// Every mbarrier wait is bounded; on expiry the kernel reports
+// RKV_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and returns.
+#include "rkv_internal.cuh"
+#include "umma.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace rkv {
+
+enum { M_P = 0, M_DIST = 1, M_S1 = 2, M_S2 = 3 };
+
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
+
+struct UmmaArgs {
+    int LB, B, T, rows;   // rows: A-operand rows per lb (T, or n_ref for M_P)
+    int n_mtiles, n_ntiles, k_chunks, a_sources, b_split, b_per_layer, max_chunks;
+    int W, d_ff, d_c, n_ref, bits;
+    float *P1, *P2;
+    const float *ref_sqnorm;
+    const int32_t *pool_size, *ref_slot;
+    float2 *cand;
+    const int4 *ref_idx;
+    __nv_bfloat16 *dh_hi, *dh_lo;
+    uint8_t *codes;
+    float2 *hdr;
+    float *z_out;
+    int32_t *status;
+};
+
+struct Item { int lb, m, n0, n1, chunk; };
+
+template <int MODE>
+__device__ __forceinline__ int item_count(const UmmaArgs &a)
+{
+    return a.LB * a.n_mtiles * (MODE == M_DIST ? a.max_chunks : a.n_ntiles);
+}
+
+// Work item i -> (lb, token tile, N-tile range).  Distance items visit the late
+// (largest-pool) token tiles first.
+template <int MODE>
+__device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, Item &it)
+{
+    if (MODE == M_DIST) {
+        const int chunk = i % a.max_chunks, r = i / a.max_chunks;
+        const int lb = r % a.LB, m = a.n_mtiles - 1 - r / a.LB;
+        const int nt = dist_ntiles(a.pool_size, a.T, m);
+        it.lb = lb; it.m = m; it.chunk = chunk;
+        it.n0 = chunk * kDistChunk;
+        it.n1 = min(nt, it.n0 + kDistChunk);
+        return it.n0 < it.n1;
+    }
+    const int n = i % a.n_ntiles, r = i / a.n_ntiles;
+    it.lb = r % a.LB; it.m = r / a.LB; it.chunk = 0;
+    it.n0 = n; it.n1 = n + 1;
+    return true;
+}
+
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float (&v)[8])
+{
+    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
+    *(uint4 *)dst = *(const uint4 *)o;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+       const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+       const UmmaArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = smem_raw + ((1024u - (um::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = (uint64_t *)(tiles + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            um::mbar_init(&full[s], 1);
+            um::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            um::mbar_init(&tfull[b], 1);
+            um::mbar_init(&tempty[b], 128);
+        }
+        um::mbar_init(drain, 1);
+        *abort_flag = 0;
+        um::fence_mbar_init();
+    }
+    if (warp == 1) {
+        um::tmem_alloc(tmem_slot, 512);
+        um::tmem_relinquish();
+    }
+    um::tc_fence_before();
+    __syncthreads();
+    um::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_items = item_count<MODE>(a);
+    const int k_iters = a.k_chunks * a.a_sources;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            um::prefetch_tmap(&tmA0);
+            um::prefetch_tmap(&tmA1);
+            um::prefetch_tmap(&tmB0);
+            um::prefetch_tmap(&tmB1);
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t last_ph[kStages];
+            bool used[kStages];
+            for (int s = 0; s < kStages; ++s) { used[s] = false; last_ph[s] = 0; }
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                Item it;
+                if (!item_get<MODE>(a, i, it)) continue;
+                const int bz = a.b_per_layer ? it.lb / a.B : it.lb;
+                for (int n = it.n0; n < it.n1 && ok; ++n) {
+                    for (int kc = 0; kc < k_iters; ++kc) {
+                        if (*abort_flag || !um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sa = tiles + stage * kStageBytes;
+                        uint8_t *sb = sa + kABytes;
+                        um::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                        const int src = kc / a.k_chunks;
+                        const int kx = (kc - src * a.k_chunks) * kBK;
+                        um::tma_load_3d(sa, src ? &tmA1 : &tmA0, &full[stage], kx, it.m * kBM, it.lb);
+                        if (a.b_split) {
+                            um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * (kBN / 2), bz);
+                            um::tma_load_3d(sb + kBBytes / 2, &tmB1, &full[stage], kx, n * (kBN / 2), bz);
+                        } else {
+                            um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * kBN, bz);
+                        }
+                        used[stage] = true;
+                        last_ph[stage] = ph;
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every issued copy must land before the CTA may exit
+            for (int s = 0; s < kStages; ++s)
+                if (used[s]) um::mbar_wait(&full[s], last_ph[s], kWaitCycles);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0, cnt = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                Item it;
+                if (!item_get<MODE>(a, i, it)) continue;
+                for (int n = it.n0; n < it.n1 && ok; ++n) {
+                    const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
+                    if (*abort_flag || !um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles)) {
+                        ok = false;
+                        break;
+                    }
+                    um::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kBN;
+                    for (int kc = 0; kc < k_iters; ++kc) {
+                        if (*abort_flag || !um::mbar_wait(&full[stage], ph, kWaitCycles)) {
+                            ok = false;
+                            break;
+                        }
+                        um::tc_fence_after();
+                        const uint32_t sa = um::smem_u32(tiles + stage * kStageBytes);
+                        const uint64_t ad = um::sdesc_sw128(sa);
+                        const uint64_t bd = um::sdesc_sw128(sa + kABytes);
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)
+                            um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                        um::mma_commit(&empty[stage]);
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    um::mma_commit(&tfull[buf]);
+                    ++cnt;
+                }
+            }
+            if (!ok) {
+                set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // all issued MMAs complete before TMEM can be released
+            um::mma_commit(drain);
+            um::mbar_wait(drain, 0, kWaitCycles);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lanes [32q, 32q+32) belong to this warp
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint32_t cnt = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            Item it;
+            if (!item_get<MODE>(a, i, it)) continue;
+            const int r = it.m * kBM + row;
+            const bool in = r < a.rows;
+
+            float be[kCand];
+            int bs[kCand];
+            int pool = 0, tile_pool = 0;
+            if (MODE == M_DIST) {
+#pragma unroll
+                for (int j = 0; j < kCand; ++j) { be[j] = INFINITY; bs[j] = -1; }
+                pool = in ? a.pool_size[r] : 0;
+                tile_pool = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1];
+            }
+            int sl[4] = {-1, -1, -1, -1};
+            int kk = 0;
+            bool is_ref = true;
+            if (MODE == M_S1 || MODE == M_S2) {
+                is_ref = in ? (a.ref_slot[r] >= 0) : true;
+                if (MODE == M_S1 && in && !is_ref) {
+                    int4 ix = a.ref_idx[(size_t)it.lb * a.T + r];
+                    sl[0] = ix.x; sl[1] = ix.y; sl[2] = ix.z; sl[3] = ix.w;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (sl[j] >= 0) ++kk;
+                }
+            }
+
+            for (int n = it.n0; n < it.n1; ++n) {
+                const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
+                bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                um::tc_fence_after();
+                const uint32_t tb = tl + buf * kBN;
+
+                if (MODE == M_P) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+                        float v1[32], v2[32];
+                        um::tmem_ld32(tb + c0, v1);
+                        um::tmem_ld32(tb + kBN / 2 + c0, v2);
+                        const int f0 = n * (kBN / 2) + c0;
+                        if (in && f0 < a.d_ff) {
+                            float4 *p1 = (float4 *)(a.P1 + ((size_t)it.lb * a.n_ref + r) * a.d_ff + f0);
+                            float4 *p2 = (float4 *)(a.P2 + ((size_t)it.lb * a.n_ref + r) * a.d_ff + f0);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                p1[j] = make_float4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
+                                p2[j] = make_float4(v2[4 * j], v2[4 * j + 1], v2[4 * j + 2], v2[4 * j + 3]);
+                            }
+                        }
+                    }
+                } else if (MODE == M_DIST) {
+                    const float *rn = a.ref_sqnorm + (size_t)it.lb * a.n_ref;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < kBN; c0 += 32) {
+                        const int s0 = n * kBN + c0;
+                        if (s0 >= tile_pool) break;          // uniform over the CTA
+                        float v[32];
+                        um::tmem_ld32(tb + c0, v);
+                        const float rn_l = (s0 + lane < a.n_ref) ? rn[s0 + lane] : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float rj = __shfl_sync(0xffffffffu, rn_l, j);
+                            const float e = fmaf(-2.0f, v[j], rj);
+                            if (s0 + j < pool && e < be[kCand - 1]) {
+                                // slots arrive in increasing order: strict < keeps the
+                                // lower slot ahead of an equal later one
+                                float ce = e;
+                                int cs = s0 + j;
+#pragma unroll
+                                for (int qq = 0; qq < kCand; ++qq) {
+                                    const bool lt = ce < be[qq];
+                                    const float te = lt ? be[qq] : ce;
+                                    const int ts = lt ? bs[qq] : cs;
+                                    if (lt) { be[qq] = ce; bs[qq] = cs; }
+                                    ce = te;
+                                    cs = ts;
+                                }
+                            }
+                        }
+                    }
+                } else if (MODE == M_S1) {
+                    const size_t pbase = (size_t)it.lb * a.n_ref;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+                        float v1[32], v2[32];
+                        um::tmem_ld32(tb + c0, v1);
+                        um::tmem_ld32(tb + kBN / 2 + c0, v2);
+                        const int f0 = n * (kBN / 2) + c0;
+                        if (!in || f0 >= a.d_ff) continue;
+                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
+                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
+#pragma unroll
+                        for (int s8 = 0; s8 < 4; ++s8) {
+                            float p1[8] = {0, 0, 0, 0, 0, 0, 0, 0}, p2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (sl[j] < 0) continue;
+                                const float4 *q1 = (const float4 *)(a.P1 + (pbase + sl[j]) * a.d_ff + f0 + 8 * s8);
+                                const float4 *q2 = (const float4 *)(a.P2 + (pbase + sl[j]) * a.d_ff + f0 + 8 * s8);
+                                const float4 x0 = __ldg(q1), x1 = __ldg(q1 + 1);
+                                const float4 y0 = __ldg(q2), y1 = __ldg(q2 + 1);
+                                p1[0] += x0.x; p1[1] += x0.y; p1[2] += x0.z; p1[3] += x0.w;
+                                p1[4] += x1.x; p1[5] += x1.y; p1[6] += x1.z; p1[7] += x1.w;
+                                p2[0] += y0.x; p2[1] += y0.y; p2[2] += y0.z; p2[3] += y0.w;
+                                p2[4] += y1.x; p2[5] += y1.y; p2[6] += y1.z; p2[7] += y1.w;
+                            }
+                            float dh[8], h8[8], l8[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float m1 = p1[j], m2 = p2[j];
+                                if (kk > 0) { m1 = __fdiv_rn(m1, (float)kk); m2 = __fdiv_rn(m2, (float)kk); }
+                                const float x1v = v1[8 * s8 + j], x2v = v2[8 * s8 + j];
+                                dh[j] = is_ref ? 0.0f : silu(x1v) * x2v - silu(m1) * m2;
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh[j]);
+                                h8[j] = __bfloat162float(hb);
+                                l8[j] = dh[j] - h8[j];
+                            }
+                            store_bf16x8(hi + 8 * s8, h8);
+                            store_bf16x8(lo + 8 * s8, l8);
+                        }
+                    }
+                } else {  // M_S2
+#pragma unroll 1
+                    for (int g8 = 0; g8 < kBN / 32; ++g8) {
+                        const int c0 = n * kBN + g8 * 32;
+                        if (c0 >= a.d_c) break;              // uniform
+                        float v[32];
+                        um::tmem_ld32(tb + g8 * 32, v);
+                        if (!in) continue;
+                        if (is_ref) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        }
+                        uint32_t wq[4];
+                        float zmin, delta;
+                        quant_group32(v, a.bits, wq, zmin, delta);
+                        const size_t rec = (size_t)it.lb * a.T + r;
+                        const int g = c0 >> 5;
+                        uint8_t *dst = a.codes + rec * (size_t)(a.d_c * a.bits / 8) + g * (a.bits * 4);
+                        if (a.bits == 4) *(uint4 *)dst = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        else *(uint2 *)dst = make_uint2(wq[0], wq[1]);
+                        a.hdr[rec * (a.d_c / 32) + g] = make_float2(zmin, delta);
+                        if (a.z_out) {
+                            float4 *zo = (float4 *)(a.z_out + rec * a.d_c + c0);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                zo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                    }
+                }
+                um::tc_fence_before();
+                um::mbar_arrive(&tempty[buf]);
+                ++cnt;
+            }
+            if (MODE == M_DIST && ok && in) {
+                float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand);
+#pragma unroll
+                for (int j = 0; j < kCand / 2; ++j)
+                    cp[j] = make_float4(be[2 * j], __int_as_float(bs[2 * j]), be[2 * j + 1],
+                                        __int_as_float(bs[2 * j + 1]));
+            }
+        }
+        if (!ok) {
+            set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+
+    um::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        um::tc_fence_after();
+        um::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// bf16 [batch][rows][inner] row-major, box = 64 (inner) x box_rows, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                     uint64_t batch, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
+                       const CUtensorMap &b1, const UmmaArgs &args, cudaStream_t s)
+{
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_umma<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const long long items =
+        (long long)args.LB * args.n_mtiles * (MODE == M_DIST ? args.max_chunks : args.n_ntiles);
+    if (items <= 0) return cudaSuccess;
+    const int sms = device_sm_count();
+    const int grid = (int)(items < sms ? items : sms);
+    static const char *names[4] = {"umma_ref_proj", "umma_distance_topk", "umma_swiglu_diff",
+                                   "umma_z_quant"};
+    ProfScope prof(names[MODE], s);
+    k_umma<MODE><<<grid, 192, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
+                                 const void *W1t, const void *W2t, const void *W3t,
+                                 const rkv_cache *cache, uint8_t *ws, const Workspace &wl,
+                                 float *z_out, int32_t *status, cudaStream_t s)
+{
+    cudaError_t e;
+    float *P1 = (float *)(ws + wl.P1), *P2 = (float *)(ws + wl.P2);
+    float *rn_max = (float *)(ws + wl.rn_max);
+    float2 *cand = (float2 *)(ws + wl.cand);
+    __nv_bfloat16 *dh_hi = (__nv_bfloat16 *)(ws + wl.dh_hi);
+    __nv_bfloat16 *dh_lo = (__nv_bfloat16 *)(ws + wl.dh_lo);
+    const bool fp8 = g.ref_dtype == RKV_FP8_E4M3;
+    void *ref_mma = fp8 ? (void *)(ws + wl.ref_mma) : pool->ref_vec;
+    if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, s)) != cudaSuccess) return e;
+
+    UmmaArgs a{};
+    a.LB = g.LB; a.B = g.B; a.T = g.T; a.W = g.W; a.d_ff = g.d_ff; a.d_c = g.d_c;
+    a.n_ref = g.n_ref; a.bits = g.bits; a.max_chunks = g.max_chunks;
+    a.P1 = P1; a.P2 = P2; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
+    a.ref_slot = pool->ref_slot; a.cand = cand; a.ref_idx = (const int4 *)cache->ref_idx;
+    a.dh_hi = dh_hi; a.dh_lo = dh_lo; a.codes = cache->codes; a.hdr = (float2 *)cache->hdr;
+    a.z_out = z_out; a.status = status;
+    const int kw = (g.W + kBK - 1) / kBK;
+
+    CUtensorMap mX, mW1, mW2, mW3, mHi, mLo, mRa, mRb;
+    if (!make_map(&mX, kv, g.W, g.T, g.LB, kBM) || !make_map(&mW1, W1t, g.W, g.d_ff, g.L, kBN / 2) ||
+        !make_map(&mW2, W2t, g.W, g.d_ff, g.L, kBN / 2) ||
+        !make_map(&mW3, W3t, g.d_ff, g.d_c, g.L, kBN) ||
+        !make_map(&mHi, dh_hi, g.d_ff, g.T, g.LB, kBM) ||
+        !make_map(&mLo, dh_lo, g.d_ff, g.T, g.LB, kBM))
+        return cudaErrorInvalidValue;
+
+    if (g.n_ref > 0) {
+        if (!make_map(&mRa, ref_mma, g.W, g.n_ref, g.LB, kBM) ||
+            !make_map(&mRb, ref_mma, g.W, g.n_ref, g.LB, kBN))
+            return cudaErrorInvalidValue;
+        // P1 | P2 for every reference
+        UmmaArgs p = a;
+        p.rows = g.n_ref; p.n_mtiles = (g.n_ref + kBM - 1) / kBM; p.n_ntiles = (g.d_ff + 127) / 128;
+        p.k_chunks = kw; p.a_sources = 1; p.b_split = 1; p.b_per_layer = 1;
+        if ((e = run<M_P>(mRa, mRa, mW1, mW2, p, s)) != cudaSuccess) return e;
+        // distance expansion and per-item candidates
+        UmmaArgs d = a;
+        d.rows = g.T; d.n_mtiles = g.n_mtiles; d.n_ntiles = 1;
+        d.k_chunks = kw; d.a_sources = 1; d.b_split = 0; d.b_per_layer = 0;
+        if ((e = run<M_DIST>(mX, mX, mRb, mRb, d, s)) != cudaSuccess) return e;
+    }
+    if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, rn_max, cache->ref_idx, status,
+                                  s)) != cudaSuccess)
+        return e;
+    {
+        UmmaArgs p = a;
+        p.rows = g.T; p.n_mtiles = g.n_mtiles; p.n_ntiles = (g.d_ff + 127) / 128;
+        p.k_chunks = kw; p.a_sources = 1; p.b_split = 1; p.b_per_layer = 1;
+        if ((e = run<M_S1>(mX, mX, mW1, mW2, p, s)) != cudaSuccess) return e;
+    }
+    {
+        UmmaArgs p = a;
+        p.rows = g.T; p.n_mtiles = g.n_mtiles; p.n_ntiles = (g.d_c + kBN - 1) / kBN;
+        p.k_chunks = (g.d_ff + kBK - 1) / kBK; p.a_sources = 2; p.b_split = 0; p.b_per_layer = 1;
+        if ((e = run<M_S2>(mHi, mLo, mW3, mW3, p, s)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace rkv

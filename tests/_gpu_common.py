@@ -1,0 +1,171 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI on
+seeded inputs, unpack its records, and compare them with the fp64 oracle under the
+tolerances of the write path:
+  * reference indices bit-exact, except tokens whose oracle k-th and (k+1)-th
+    distances lie within 1e-5 relative (then the GPU set must still be a valid
+    nearest set within that band);
+  * z within 2e-2 of the token's max |z| (floored at 1e-3 of the config's max |z|);
+  * codes equal except +-1 on at most 0.1% of coordinates, and only where the
+    oracle's (z - z_min)/delta lies within the z discrepancy of a rounding boundary.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import rkv_workload as wl
+from reference_residual_kv_gb300 import build, rkv
+
+TIE_BAND = 1e-5
+Z_TOL = 2e-2
+CODE_BUDGET = 1e-3
+
+
+def ensure_lib():
+    build.build()
+    rkv.lib()
+
+
+def gen_inputs(cfg: wl.Config, layers=None):
+    """Stored kv [L][B][T][W] and weights (lists per layer), generated in threads."""
+    layers = list(range(cfg.L)) if layers is None else layers
+    with cf.ThreadPoolExecutor(max_workers=min(16, len(layers))) as ex:
+        kv = list(ex.map(lambda l: wl.layer_kv(cfg, l), layers))
+        w = list(ex.map(lambda l: wl.layer_weights(cfg, l), layers))
+    return kv, w
+
+
+def to_device(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def run_gpu(cfg: wl.Config, kv, w, want_z=True):
+    """Build pool + compress through the C ABI; returns (Buffers, device inputs)."""
+    ensure_lib()
+    p = rkv.params_from_config(cfg)
+    bufs = rkv.Buffers(p, want_z=want_z)
+    kv_d = to_device(np.stack(kv), cfg.kv_dtype)
+    W1 = to_device(np.stack([x[0] for x in w]), cfg.kv_dtype)
+    W2 = to_device(np.stack([x[1] for x in w]), cfg.kv_dtype)
+    W3 = to_device(np.stack([x[2] for x in w]), cfg.kv_dtype)
+    bufs.build_ref_pool(kv_d)
+    bufs.compress(kv_d, W1, W2, W3)
+    torch.cuda.synchronize()
+    return bufs, (kv_d, W1, W2, W3)
+
+
+def unpack_codes(codes: np.ndarray, bits: int, d_c: int) -> np.ndarray:
+    c = codes.astype(np.uint8)
+    if bits == 4:
+        q = np.stack([c & 15, c >> 4], axis=-1)
+    else:
+        q = np.stack([(c >> (2 * i)) & 3 for i in range(4)], axis=-1)
+    return q.reshape(*codes.shape[:-1], d_c)
+
+
+def host_records(cfg, bufs):
+    """GPU records as numpy: ref_idx [LB][T][4], q [LB][T][d_c], hdr [LB][T][G][2], z."""
+    out = dict(idx=bufs.ref_idx.cpu().numpy(), hdr=bufs.hdr.cpu().numpy(),
+               q=unpack_codes(bufs.codes.cpu().numpy(), cfg.bits, cfg.d_c))
+    if bufs.z is not None:
+        out["z"] = bufs.z.cpu().numpy()
+    return out
+
+
+def check_tokens(cfg, kv_seq, w_layer, gpu, lb, tokens, zmax_cfg=None, report=None):
+    """Compare one (layer, sequence)'s GPU records for `tokens` with the oracle."""
+    tokens = np.asarray(tokens, dtype=np.int32)
+    o = oracle.compress_tokens(cfg, kv_seq, w_layer, tokens)
+    ref_pos = oracle.schedule(cfg)
+    gidx = gpu["idx"][lb][tokens][:, : cfg.k]
+    exempt = np.zeros(tokens.size, bool)
+    mism = np.nonzero(np.any(gidx != o["idx"], axis=1))[0]
+    refs64 = None
+    for n in mism:
+        dk, dk1 = o["dk"][n]
+        assert dk1 - dk <= TIE_BAND * max(dk, 1e-300), (
+            "token %d: GPU refs %s, oracle %s, gap %.3g (d_k %.6g)" % (tokens[n], gidx[n], o["idx"][n], dk1 - dk, dk))
+        if refs64 is None:
+            refs64, _ = oracle.stored_refs(cfg, kv_seq, ref_pos)
+        x = wl.stored_to_f64(kv_seq[tokens[n]], cfg.kv_dtype)
+        for s in gidx[n][gidx[n] >= 0]:
+            assert oracle.sqdist(x, refs64[s]) <= dk * (1 + TIE_BAND) + 1e-300
+        exempt[n] = True
+    keep = ~exempt
+    zo = o["z"][keep]
+    zg = None
+    if "z" in gpu:
+        zg = gpu["z"][lb][tokens][keep]
+    zscale = np.maximum(np.abs(zo).max(axis=1, initial=0.0),
+                        1e-3 * (zmax_cfg if zmax_cfg is not None else np.abs(zo).max(initial=0.0)))
+    if zg is not None:
+        err = np.abs(zg - zo).max(axis=1, initial=0.0)
+        bad = err > Z_TOL * zscale
+        assert not bad.any(), "z mismatch at tokens %s: err %s scale %s" % (
+            tokens[keep][bad][:5], err[bad][:5], zscale[bad][:5])
+    # group extremes
+    G = cfg.d_c // 32
+    hdr = gpu["hdr"][lb][tokens][keep]
+    np.testing.assert_allclose(hdr[..., 0], o["zmin"][keep], rtol=0,
+                               atol=float(np.max(Z_TOL * zscale, initial=0.0)) + 1e-30)
+    # codes: +-1 only near a rounding boundary
+    qg = gpu["q"][lb][tokens][keep].astype(int)
+    qo = o["q"][keep].astype(int)
+    diff = qg != qo
+    n_diff = int(diff.sum())
+    if n_diff:
+        assert np.all(np.abs(qg - qo)[diff] == 1), "code differs by more than 1"
+        rows, cols = np.nonzero(diff)
+        g = cols // 32
+        dl_o = o["delta"][keep][rows, g]
+        mn_o = o["zmin"][keep][rows, g]
+        u = (zo[rows, cols] - mn_o) / dl_o
+        frac = u - np.floor(u)
+        if zg is not None:
+            dz = np.abs(zg[rows, cols] - zo[rows, cols])
+        else:
+            dz = Z_TOL * zscale[rows]
+        dmin = np.abs(hdr[rows, g, 0] - mn_o)
+        ddl = np.abs(hdr[rows, g, 1] - dl_o)
+        slack = (dz + dmin + qo[rows, cols] * ddl) / dl_o + 1e-6
+        assert np.all(np.abs(frac - 0.5) <= slack), "code flip away from a rounding boundary"
+    if report is not None:
+        report["coords"] = report.get("coords", 0) + int(qo.size)
+        report["flips"] = report.get("flips", 0) + n_diff
+        report["exempt"] = report.get("exempt", 0) + int(exempt.sum())
+        report["tokens"] = report.get("tokens", 0) + int(tokens.size)
+        if zg is not None and zo.size:
+            rel = (np.abs(zg - zo).max(axis=1) / zscale).max()
+            report["max_rel_z"] = max(report.get("max_rel_z", 0.0), float(rel))
+    return o
+
+
+def check_all_indices(cfg, kv_seq, gpu_idx_seq, tokens=None, report=None):
+    """Reference sets of `tokens` (default: every token) against the oracle's retrieval."""
+    tokens = np.arange(cfg.T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
+    idx, ki, dk = oracle.retrieve_tokens(cfg, kv_seq, tokens)
+    g = gpu_idx_seq[tokens][:, : cfg.k]
+    assert np.all(gpu_idx_seq[tokens][:, cfg.k:] == -1)
+    bad = np.nonzero(np.any(g != idx, axis=1))[0]
+    for n in bad:
+        assert dk[n, 1] - dk[n, 0] <= TIE_BAND * max(dk[n, 0], 1e-300), (
+            "token %d: GPU %s oracle %s (d_k %.8g, d_k+1 %.8g)" % (tokens[n], g[n], idx[n], dk[n, 0], dk[n, 1]))
+    if report is not None:
+        report["idx_exempt"] = report.get("idx_exempt", 0) + int(bad.size)
+        report["idx_tokens"] = report.get("idx_tokens", 0) + int(tokens.size)
+    return int(bad.size)
+
+
+def sample_tokens(cfg, n, seed):
+    """Edge tokens (first few, tile boundaries, last ones) plus a random sample."""
+    T = cfg.T
+    edge = [t for t in (1, 2, 3, 7, 9, 15, 17, 31, 33, 63, 127, 129, 255, 257, T - 2, T - 1) if 0 <= t < T]
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(T, size=min(n, T), replace=False)
+    return np.unique(np.concatenate([edge, rest])).astype(np.int32)

@@ -1,0 +1,88 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point that
+include/rkv.h declares; host-only calls validate arguments without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from reference_residual_kv_gb300 import build, rkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(rkv_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return rkv.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("rkv_build_ref_pool", "rkv_compress", "rkv_gather_dequant", "rkv_query_sizes"):
+        assert n in names
+    assert set(names) == set(rkv.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_query_sizes_host_only(lib):
+    p = rkv.make_params(32, 1, 8192, 8, 128, 1024, 512, stride=8)
+    assert rkv.rkv_n_ref(p) == 1024
+    pool, cache, ws = rkv.rkv_query_sizes(p)
+    assert cache == 32 * 8192 * (256 + 16 * 8 + 16)
+    assert pool == 1024 * 4 + 2 * 8192 * 4 + 32 * 1024 * 2048 * 2 + 32 * 1024 * 4
+    assert ws > 0
+    p8 = rkv.make_params(1, 1, 131072, 8, 128, 1024, 512, stride=16, ref_dtype="fp8")
+    assert rkv.rkv_n_ref(p8) == 8192
+    assert rkv.rkv_query_sizes(p8)[0] == 8192 * 4 + 2 * 131072 * 4 + 8192 * 2048 + 8192 * 4
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("bits", 3, rkv.RKV_ERR_INVALID_ARG),
+    ("T", 0, rkv.RKV_ERR_INVALID_ARG),
+    ("stride", 0, rkv.RKV_ERR_INVALID_ARG),
+    ("k", 5, rkv.RKV_ERR_UNSUPPORTED),
+    ("group", 16, rkv.RKV_ERR_UNSUPPORTED),
+    ("d_c", 48, rkv.RKV_ERR_UNSUPPORTED),
+    ("ref_dtype", rkv.RKV_FP8_E4M3, rkv.RKV_ERR_INVALID_ARG),   # FP8 refs need bf16 kv
+])
+def test_invalid_params_rejected_before_any_launch(lib, field, value, code):
+    p = rkv.make_params(1, 1, 256, 2, 64, 256, 64, kv_dtype="f32")
+    setattr(p, field, value)
+    a = ctypes.c_size_t()
+    assert lib.rkv_query_sizes(ctypes.byref(p), ctypes.byref(a), None, None) == code
+    pool = rkv.rkv_ref_pool(16, 16, 16, 16, 16)
+    # validation fails before anything touches the device (no GPU here)
+    assert lib.rkv_build_ref_pool(ctypes.byref(p), 16, ctypes.byref(pool), None) == code
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    p = rkv.make_params(1, 1, 256, 2, 64, 256, 64, kv_dtype="f32")
+    pool = rkv.rkv_ref_pool(16, 16, 16, 16, 16)
+    assert lib.rkv_build_ref_pool(ctypes.byref(p), None, ctypes.byref(pool), None) == rkv.RKV_ERR_INVALID_ARG
+    assert lib.rkv_build_ref_pool(ctypes.byref(p), 24, ctypes.byref(pool), None) == rkv.RKV_ERR_ALIGNMENT
+    cache = rkv.rkv_cache(16, 16, 16)
+    st = lib.rkv_compress(ctypes.byref(p), 16, ctypes.byref(pool), 16, 16, 16, ctypes.byref(cache),
+                          None, 0, None, 16, None)
+    assert st == rkv.RKV_ERR_WORKSPACE
+    st = lib.rkv_gather_dequant(ctypes.byref(p), ctypes.byref(pool), ctypes.byref(cache), 16, 4,
+                                16, 16, 7, 16, None)
+    assert st == rkv.RKV_ERR_INVALID_ARG
+    assert lib.rkv_status_string(rkv.RKV_ERR_INDEX) == b"index out of range (device)"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(rkv, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(rkv, "_lib", None)
+    with pytest.raises(RuntimeError):
+        rkv.lib()

@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs.  Small cases check every token's reference set and a sample of
+tokens' codes; full-size configs (launched as the benchmark launches them: all layers
+in one call) check sampled tokens of several layers.  Read-path tests check the
+gather against the records it reads and against the oracle's means, that it never
+reads an unselected token, and that bad indices are reported, not faulted on."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rkv_workload as wl
+from reference_residual_kv_gb300 import rkv
+
+from _gpu_common import (CODE_BUDGET, check_all_indices, check_tokens, gen_inputs, host_records,
+                         run_gpu, sample_tokens, to_device, unpack_codes)
+
+pytestmark = pytest.mark.gpu
+
+C = wl.CONFIGS
+
+
+def _parity(cfg, n_sample=120, layers_checked=None, all_idx=True, seed=0):
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w)
+    assert bufs.device_status() == 0
+    gpu = host_records(cfg, bufs)
+    report = {}
+    zmax = float(np.abs(gpu["z"]).max())
+    layers_checked = range(cfg.L) if layers_checked is None else layers_checked
+    for l in layers_checked:
+        for b in range(cfg.B):
+            lb = l * cfg.B + b
+            if all_idx:
+                check_all_indices(cfg, kv[l][b], gpu["idx"][lb], report=report)
+            toks = sample_tokens(cfg, n_sample, seed + lb)
+            if not all_idx:
+                check_all_indices(cfg, kv[l][b], gpu["idx"][lb], tokens=toks, report=report)
+            check_tokens(cfg, kv[l][b], w[l], gpu, lb, toks, zmax_cfg=zmax, report=report)
+    assert report["flips"] <= CODE_BUDGET * report["coords"], report
+    print(cfg.name, report)
+    return bufs, kv, w, gpu, report
+
+
+# ------------------------------------------------------------------ write path
+def test_tiny_fp32_every_token():
+    cfg = C["tiny-fp32"]
+    bufs, kv, w, gpu, rep = _parity(cfg, n_sample=cfg.T)
+    assert rep["tokens"] == cfg.T and rep["max_rel_z"] < 1e-4
+
+
+SMALL = {
+    "llama-2x1000": C["llama3.1-8b-kv"].replace(L=2, T=1000),
+    "qwen-1x777": C["qwen2.5-7b-kv"].replace(L=1, T=777),
+    "long-fp8-1x1500": C["long-131k-fp8ref"].replace(T=1500),
+    "mm-int2-2x4096": C["multimodal-8x4096-int2"].replace(B=2),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_bf16_small_ragged(name):
+    cfg = SMALL[name]
+    _parity(cfg, n_sample=100, all_idx=True)
+
+
+@pytest.mark.parametrize("name,layers", [
+    ("llama3.1-8b-kv", [0, 17, 31]),
+    ("qwen2.5-7b-kv", [0, 27]),
+    ("long-131k-fp8ref", [0]),
+    ("multimodal-8x4096-int2", [0]),
+])
+def test_full_size_sampled(name, layers):
+    cfg = C[name]
+    n = 60 if cfg.T > 10000 else 80
+    _parity(cfg, n_sample=n, layers_checked=layers, all_idx=False)
+
+
+def test_edge_cases_small_T_first_offset_k():
+    base = C["llama3.1-8b-kv"].replace(L=1, N=2, D=64, d_ff=256, d_c=64)
+    for cfg in (base.replace(T=1), base.replace(T=9), base.replace(T=130),
+                base.replace(T=300, first=5), base.replace(T=300, k=1),
+                base.replace(T=300, k=2, bits=2)):
+        bufs, kv, w, gpu, rep = _parity(cfg, n_sample=cfg.T)
+        if cfg.first > 0:
+            # tokens before the first reference have an empty pool: no refs, z = f_c(kv)
+            assert np.all(gpu["idx"][0][: cfg.first] == -1)
+
+
+def test_constant_group_and_ties():
+    # token 3 is a copy of reference 0 (its only pool member): z = 0 exactly and
+    # every group is constant; references 5, 6, 7 duplicate reference 4, so the
+    # lower slots win the ties.
+    cfg = C["llama3.1-8b-kv"].replace(L=1, T=512, N=2, D=64, d_ff=256, d_c=64)
+    kv, w = gen_inputs(cfg)
+    kv[0] = kv[0].copy()
+    kv[0][0, 3] = kv[0][0, 0]
+    for s in (5, 6, 7):
+        kv[0][0, 8 * s] = kv[0][0, 32]
+    kv[0][0, 300] = kv[0][0, 32]
+    bufs, _ = run_gpu(cfg, kv, w)
+    gpu = host_records(cfg, bufs)
+    assert np.all(gpu["z"][0, 3] == 0) and np.all(gpu["hdr"][0, 3] == 0) and np.all(gpu["q"][0, 3] == 0)
+    assert gpu["idx"][0, 300].tolist() == [4, 5, 6, 7]
+    check_all_indices(cfg, kv[0][0], gpu["idx"][0])
+    check_tokens(cfg, kv[0][0], w[0], gpu, 0, np.array([3, 300, 301]))
+
+
+def test_records_requantise_bit_exactly_from_gpu_z():
+    # the kernels' own quantisation decision, repeated on the host in fp32 with the
+    # same operations, reproduces every code and group header bit for bit
+    cfg = SMALL["llama-2x1000"]
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w)
+    gpu = host_records(cfg, bufs)
+    z = gpu["z"].reshape(-1, cfg.d_c // 32, 32).astype(np.float32)
+    lo, hi = z.min(-1), z.max(-1)
+    qmax = np.float32((1 << cfg.bits) - 1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        dl = (hi - lo) / qmax
+        u = (z - lo[..., None]) / dl[..., None] + np.float32(0.5)
+    q = np.clip(np.floor(u), 0, qmax)
+    q = np.where((hi == lo)[..., None], 0, q).astype(np.uint8)
+    dl = np.where(hi == lo, np.float32(0), dl)
+    assert np.array_equal(q.reshape(gpu["q"].shape), gpu["q"])
+    hdr = gpu["hdr"].reshape(-1, cfg.d_c // 32, 2)
+    assert np.array_equal(hdr[..., 0], lo) and np.array_equal(hdr[..., 1], dl)
+
+
+# ------------------------------------------------------------------ read path
+def _host_dequant(cfg, gpu, lb, sel):
+    q = gpu["q"][lb][sel].astype(np.float64)
+    h = gpu["hdr"][lb][sel].astype(np.float64)
+    g = np.arange(cfg.d_c) // 32
+    return q * h[:, g, 1] + h[:, g, 0]
+
+
+@pytest.mark.parametrize("name,out", [("tiny-fp32", "f32"), ("llama-2x1000", "bf16"),
+                                      ("long-fp8-1x1500", "bf16"), ("mm-int2-2x4096", "bf16")])
+def test_gather_matches_records_and_oracle_means(name, out):
+    cfg = C[name] if name in C else SMALL[name]
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w)
+    gpu = host_records(cfg, bufs)
+    LB = cfg.L * cfg.B
+    sels = [np.sort(np.random.default_rng(lb).choice(cfg.T, size=min(300, cfg.T), replace=False))
+            for lb in range(LB)]
+    n_sel = len(sels[0])
+    sel = torch.tensor(np.stack(sels), dtype=torch.int32, device="cuda")
+    odt = torch.float32 if out == "f32" else torch.bfloat16
+    out_z = torch.empty((LB, n_sel, cfg.d_c), dtype=odt, device="cuda")
+    out_m = torch.empty((LB, n_sel, cfg.W), dtype=odt, device="cuda")
+    bufs.gather(sel, out_z, out_m)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == 0
+    gz = out_z.float().cpu().numpy()
+    gm = out_m.float().cpu().numpy()
+    ulp = 2.0 ** -23 if out == "f32" else 2.0 ** -8
+    for lb in range(LB):
+        l, b = divmod(lb, cfg.B)
+        # z~ exactly as the records say (one rounding to the output type)
+        ref = _host_dequant(cfg, gpu, lb, sels[lb])
+        np.testing.assert_allclose(gz[lb], ref, rtol=ulp, atol=1e-30)
+        # reference means against the oracle's (same reference sets: checked above)
+        toks = sels[lb][:80]
+        o = oracle.compress_tokens(cfg, kv[l][b], w[l], toks, want_mean=True)
+        same = np.all(gpu["idx"][lb][toks][:, : cfg.k] == o["idx"], axis=1)
+        assert same.mean() > 0.95
+        np.testing.assert_allclose(gm[lb][:80][same], o["mean"][same], rtol=ulp, atol=1e-6)
+
+
+def test_gather_standalone_padding_and_isolation():
+    cfg = SMALL["long-fp8-1x1500"]
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w)
+    T = cfg.T
+    # standalone mode (every token) equals the union of sparse reads
+    allsel = torch.arange(T, dtype=torch.int32, device="cuda").view(1, T)
+    za = torch.empty((1, T, cfg.d_c), dtype=torch.bfloat16, device="cuda")
+    ma = torch.empty((1, T, cfg.W), dtype=torch.bfloat16, device="cuda")
+    bufs.gather(allsel, za, ma)
+    sel_np = wl.gather_selection(cfg, 0)
+    sel = torch.tensor(np.concatenate([sel_np, [-1, -1, -1]]), dtype=torch.int32, device="cuda").view(1, -1)
+    zs = torch.empty((1, sel.shape[1], cfg.d_c), dtype=torch.bfloat16, device="cuda")
+    ms = torch.empty((1, sel.shape[1], cfg.W), dtype=torch.bfloat16, device="cuda")
+    bufs.gather(sel, zs, ms)
+    torch.cuda.synchronize()
+    idx = torch.tensor(sel_np, device="cuda", dtype=torch.long)
+    assert torch.equal(zs[0, : len(sel_np)], za[0, idx]) and torch.equal(ms[0, : len(sel_np)], ma[0, idx])
+    assert torch.all(zs[0, len(sel_np):] == 0) and torch.all(ms[0, len(sel_np):] == 0)
+    # poison every record the selection does not name: the read must not change
+    other = torch.ones(T, dtype=torch.bool, device="cuda")
+    other[idx] = False
+    bufs.codes[0, other] = 0xFF
+    bufs.hdr[0, other] = float("nan")
+    bufs.ref_idx[0, other] = 1 << 30
+    zp, mp = torch.empty_like(zs), torch.empty_like(ms)
+    bufs.gather(sel, zp, mp)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == 0
+    assert torch.equal(zp, zs) and torch.equal(mp, ms)
+
+
+def test_gather_out_of_range_index_is_reported_not_faulted():
+    cfg = C["tiny-fp32"]
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w)
+    sel = torch.tensor([[0, 5, cfg.T, 7]], dtype=torch.int32, device="cuda")
+    oz = torch.full((1, 4, cfg.d_c), 9.0, device="cuda")
+    om = torch.full((1, 4, cfg.W), 9.0, device="cuda")
+    bufs.gather(sel, oz, om)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == rkv.RKV_ERR_INDEX
+    assert torch.all(oz[0, 2] == 0) and torch.all(om[0, 2] == 0)
+    assert torch.all(om[0, 0] != 9.0)
+    # an empty selection launches nothing
+    bufs.status.zero_()
+    rkv.rkv_gather_dequant(bufs.p, bufs.pool, bufs.cache, None, 0, None, None, rkv.RKV_F32, None)
+
+
+def test_long_context_decode_steps():
+    # the long-context workload's read side: several decode steps of 30% random
+    # tokens plus the last 512, against the records and the oracle's means
+    cfg = C["long-131k-fp8ref"]
+    kv, w = gen_inputs(cfg)
+    bufs, _ = run_gpu(cfg, kv, w, want_z=False)
+    gpu = host_records(cfg, bufs)
+    for step in range(3):
+        s = wl.gather_selection(cfg, step)
+        sel = torch.tensor(s, dtype=torch.int32, device="cuda").view(1, -1)
+        oz = torch.empty((1, s.size, cfg.d_c), dtype=torch.bfloat16, device="cuda")
+        om = torch.empty((1, s.size, cfg.W), dtype=torch.bfloat16, device="cuda")
+        bufs.gather(sel, oz, om)
+        torch.cuda.synchronize()
+        assert bufs.device_status() == 0
+        pick = np.random.default_rng(step).choice(s.size, 40, replace=False)
+        toks = s[pick]
+        ref = _host_dequant(cfg, gpu, 0, toks)
+        np.testing.assert_allclose(oz[0, pick].float().cpu().numpy(), ref, rtol=2.0 ** -8, atol=1e-30)
+        o = oracle.compress_tokens(cfg, kv[0][0], w[0], toks, want_mean=True)
+        same = np.all(gpu["idx"][0][toks][:, : cfg.k] == o["idx"], axis=1)
+        np.testing.assert_allclose(om[0, pick].float().cpu().numpy()[same], o["mean"][same],
+                                   rtol=2.0 ** -8, atol=1e-6)
