@@ -234,8 +234,10 @@ def run_ours(args, cfg):
     p = rkv.params_from_config(cfg)
     bufs = rkv.Buffers(p, device=dev)
     LB = cfg.L * cfg.B
-    sels = np.stack([wl.gather_selection(cfg, l, 0) for l in range(LB)])
-    sel = torch.from_numpy(sels).to(dev)
+    # one decode step's index set, read from every layer (as a filter layer's
+    # selection serves the sparse layers that follow it)
+    sel1 = wl.gather_selection(cfg, 0, 0)
+    sel = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(sel1, (LB, sel1.size)))).to(dev)
     n_sel = sel.shape[1]
     out_z = torch.empty((LB, n_sel, cfg.d_c), dtype=torch.bfloat16, device=dev)
     out_m = torch.empty((LB, n_sel, cfg.W), dtype=torch.bfloat16, device=dev)

@@ -43,7 +43,9 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
+        # RKV_ORACLE_LIB lets the mutation test load a deliberately broken copy
+        alt = os.environ.get("RKV_ORACLE_LIB")
+        _lib = ctypes.CDLL(alt if alt else build())
         L = _lib
         L.rkvo_fixed_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip]
         L.rkvo_fixed_schedule.restype = ctypes.c_int

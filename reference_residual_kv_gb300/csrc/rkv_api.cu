@@ -46,6 +46,7 @@ Workspace workspace_layout(const Geometry &g)
     w.P2 = take(LB * R * g.d_ff * 4);
     w.rn_max = take(LB * 4);
     w.cand = take(tc ? LB * T * g.max_chunks * kCand * 8 : 0);
+    w.copy_flag = take(LB * T);
     w.dh_hi = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh_lo = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh32 = take(tc ? 0 : LB * T * g.d_ff * 4);

@@ -49,6 +49,7 @@ struct Workspace {
     size_t P1, P2;       // f32  [LB][n_ref][d_ff]
     size_t rn_max;       // f32  [LB]
     size_t cand;         // f32x2 [LB][T][max_chunks][kCand]  (tensor-core path)
+    size_t copy_flag;    // u8   [LB][T]  1: every chosen reference equals the token
     size_t dh_hi, dh_lo; // bf16 [LB][T][d_ff]   (tensor-core path)
     size_t dh32;         // f32  [LB][T][d_ff]   (fp32 path)
     size_t z32;          // f32  [LB][T][d_c]    (fp32 path)
@@ -82,7 +83,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
 cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
                                  const float2 *cand, const float *rn_max, int32_t *ref_idx,
-                                 int32_t *status, cudaStream_t s);
+                                 uint8_t *copy_flag, int32_t *status, cudaStream_t s);
 
 int device_sm_count();
 

@@ -28,7 +28,8 @@ __global__ void __launch_bounds__(256)
 k_simt_gate(const T *__restrict__ A, int rows, int W, int d_ff, int B_,
             const T *__restrict__ W1t, const T *__restrict__ W2t, float *__restrict__ P1,
             float *__restrict__ P2, int n_ref, const int32_t *__restrict__ ref_slot,
-            const int4 *__restrict__ ref_idx, float *__restrict__ dh)
+            const int4 *__restrict__ ref_idx, const uint8_t *__restrict__ copy_flag,
+            float *__restrict__ dh)
 {
     constexpr int BM = 64, BN = 32, BK = 32;
     __shared__ float As[BK][BM + 1];
@@ -85,7 +86,7 @@ k_simt_gate(const T *__restrict__ A, int rows, int W, int d_ff, int B_,
                 P2[((size_t)lb * n_ref + r) * d_ff + f] = a2[i][j];
             } else {
                 float v = 0.0f;
-                if (ref_slot[r] < 0) {
+                if (ref_slot[r] < 0 && !copy_flag[(size_t)lb * rows + r]) {
                     int4 ix = ref_idx[(size_t)lb * rows + r];
                     int sl[4] = {ix.x, ix.y, ix.z, ix.w};
                     float p1 = 0.0f, p2 = 0.0f;
@@ -204,18 +205,20 @@ cudaError_t launch_simt_compress(const Geometry &g, const void *kv, const rkv_re
         k_simt_gate<float, 0><<<grid, 256, 0, s>>>((const float *)pool->ref_vec, g.n_ref, g.W,
                                                    g.d_ff, g.B, (const float *)W1t,
                                                    (const float *)W2t, P1, P2, g.n_ref, nullptr,
-                                                   nullptr, nullptr);
+                                                   nullptr, nullptr, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    uint8_t *copy_flag = ws + wl.copy_flag;
     if ((e = launch_topk_finalize(g, kv, pool->ref_vec, 1, pool, nullptr, rn_max,
-                                  cache->ref_idx, status, s)) != cudaSuccess)
+                                  cache->ref_idx, copy_flag, status, s)) != cudaSuccess)
         return e;
     {
         dim3 grid((g.d_ff + 31) / 32, (g.T + 63) / 64, g.LB);
         ProfScope prof("simt_swiglu_diff", s);
         k_simt_gate<float, 1><<<grid, 256, 0, s>>>(X, g.T, g.W, g.d_ff, g.B, (const float *)W1t,
                                                    (const float *)W2t, P1, P2, g.n_ref,
-                                                   pool->ref_slot, (const int4 *)cache->ref_idx, dh);
+                                                   pool->ref_slot, (const int4 *)cache->ref_idx,
+                                                   copy_flag, dh);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     {

@@ -12,6 +12,10 @@
 //     (all of the pool fits, or the 8th candidate is more than 2E behind the k-th),
 //     the candidates are re-ranked by exact distances;
 //   * else every reference of the pool is scanned with exact distances.
+// It also flags tokens that are bit-identical to every chosen reference: their mean
+// equals the token exactly, so z = 0 exactly [RKV §2.3], which the encoder then
+// writes directly (the tensor cores need not round the token's and the
+// references' projections identically, since they sit in different tile rows).
 // Exact distances sum (x - r)^2 in fp32: for bf16 data x - r is exact, each group of
 // 8 squares is added as a tree, and the warp adds its lanes as a tree.
 // Without candidates (the fp32 path) every token takes the full scan.
@@ -103,7 +107,8 @@ __global__ void __launch_bounds__(256)
 k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
                 const int32_t *__restrict__ ref_slot, const int32_t *__restrict__ pool_size,
                 const float2 *__restrict__ cand, const float *__restrict__ rn_max, int LB, int T_,
-                int W, int n_ref, int k, int max_chunks, int4 *__restrict__ ref_idx)
+                int W, int n_ref, int k, int max_chunks, int4 *__restrict__ ref_idx,
+                uint8_t *__restrict__ copy_flag)
 {
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -111,15 +116,20 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
     const int lb = (int)(gw / T_), t = (int)(gw % T_);
 
     int out[4] = {-1, -1, -1, -1};
+    int same = 0;
     const int own = ref_slot[t];
     const int pool = pool_size[t];
+    const T *x = kv + ((size_t)lb * T_ + t) * W;
+    const T *rb = refs + (size_t)lb * n_ref * W;
     if (own >= 0) {
         out[0] = own;
     } else if (pool <= k) {
-        for (int j = 0; j < pool; ++j) out[j] = j;
+        same = pool > 0;
+        for (int j = 0; j < pool; ++j) {
+            out[j] = j;
+            same &= warp_sqdist(x, rb + (size_t)j * W, W, lane) == 0.0f;
+        }
     } else {
-        const T *x = kv + ((size_t)lb * T_ + t) * W;
-        const T *rb = refs + (size_t)lb * n_ref * W;
         float be[kMaxK];
         int bs[kMaxK];
 #pragma unroll
@@ -169,6 +179,12 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
             const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
             if (nvalid > k && ce[k] - ce[k - 1] > 2.0f * E) {
                 for (int j = 0; j < k; ++j) { be[j] = ce[j]; bs[j] = cs[j]; }
+                // possibly an exact copy of all k: confirm with exact distances
+                if (xn + ce[k - 1] <= 2.0f * E) {
+                    for (int j = 0; j < k; ++j) be[j] = warp_sqdist(x, rb + (size_t)bs[j] * W, W, lane);
+                } else {
+                    be[0] = 1.0f;   // not a copy
+                }
             } else if (pool <= kCand || ce[kCand - 1] - ce[k - 1] > 2.0f * E) {
                 for (int r = 0; r < nvalid; ++r) {
                     float d = warp_sqdist(x, rb + (size_t)cs[r] * W, W, lane);
@@ -184,6 +200,8 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
                 list_insert<kMaxK>(be, bs, d, s);
             }
         }
+        same = 1;
+        for (int j = 0; j < k; ++j) same &= be[j] == 0.0f;
         // chosen slots in ascending order
         int ch[kMaxK];
 #pragma unroll
@@ -196,13 +214,16 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) out[j] = j < k ? ch[j] : -1;
     }
-    if (lane == 0) ref_idx[(size_t)lb * T_ + t] = make_int4(out[0], out[1], out[2], out[3]);
+    if (lane == 0) {
+        ref_idx[(size_t)lb * T_ + t] = make_int4(out[0], out[1], out[2], out[3]);
+        copy_flag[(size_t)lb * T_ + t] = (uint8_t)same;
+    }
 }
 
 cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
                                  const float2 *cand, const float *rn_max, int32_t *ref_idx,
-                                 int32_t *status, cudaStream_t s)
+                                 uint8_t *copy_flag, int32_t *status, cudaStream_t s)
 {
     (void)status;
     long long warps = (long long)g.LB * g.T;
@@ -211,12 +232,12 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
     if (ref_exact_is_f32)
         k_topk_finalize<float><<<blocks, 256, 0, s>>>(
             (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size, cand,
-            rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks, (int4 *)ref_idx);
+            rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks, (int4 *)ref_idx, copy_flag);
     else
         k_topk_finalize<__nv_bfloat16><<<blocks, 256, 0, s>>>(
             (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
             pool->pool_size, cand, rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks,
-            (int4 *)ref_idx);
+            (int4 *)ref_idx, copy_flag);
     return cudaGetLastError();
 }
 

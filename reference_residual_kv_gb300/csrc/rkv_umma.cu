@@ -43,6 +43,7 @@ struct UmmaArgs {
     const int32_t *pool_size, *ref_slot;
     float2 *cand;
     const int4 *ref_idx;
+    const uint8_t *copy_flag;
     __nv_bfloat16 *dh_hi, *dh_lo;
     uint8_t *codes;
     float2 *hdr;
@@ -248,6 +249,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             bool is_ref = true;
             if (MODE == M_S1 || MODE == M_S2) {
                 is_ref = in ? (a.ref_slot[r] >= 0) : true;
+                // a token equal to all its references has z = 0 exactly
+                if (MODE == M_S1 && in && !is_ref && a.copy_flag[(size_t)it.lb * a.T + r]) is_ref = true;
                 if (MODE == M_S1 && in && !is_ref) {
                     int4 ix = a.ref_idx[(size_t)it.lb * a.T + r];
                     sl[0] = ix.x; sl[1] = ix.y; sl[2] = ix.z; sl[3] = ix.w;
@@ -481,6 +484,8 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     a.n_ref = g.n_ref; a.bits = g.bits; a.max_chunks = g.max_chunks;
     a.P1 = P1; a.P2 = P2; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
     a.ref_slot = pool->ref_slot; a.cand = cand; a.ref_idx = (const int4 *)cache->ref_idx;
+    uint8_t *copy_flag = ws + wl.copy_flag;
+    a.copy_flag = copy_flag;
     a.dh_hi = dh_hi; a.dh_lo = dh_lo; a.codes = cache->codes; a.hdr = (float2 *)cache->hdr;
     a.z_out = z_out; a.status = status;
     const int kw = (g.W + kBK - 1) / kBK;
@@ -508,8 +513,8 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         d.k_chunks = kw; d.a_sources = 1; d.b_split = 0; d.b_per_layer = 0;
         if ((e = run<M_DIST>(mX, mX, mRb, mRb, d, s)) != cudaSuccess) return e;
     }
-    if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, rn_max, cache->ref_idx, status,
-                                  s)) != cudaSuccess)
+    if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, rn_max, cache->ref_idx,
+                                  copy_flag, status, s)) != cudaSuccess)
         return e;
     {
         UmmaArgs p = a;

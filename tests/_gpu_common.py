@@ -141,7 +141,7 @@ def check_tokens(cfg, kv_seq, w_layer, gpu, lb, tokens, zmax_cfg=None, report=No
         report["exempt"] = report.get("exempt", 0) + int(exempt.sum())
         report["tokens"] = report.get("tokens", 0) + int(tokens.size)
         if zg is not None and zo.size:
-            rel = (np.abs(zg - zo).max(axis=1) / zscale).max()
+            rel = (np.abs(zg - zo).max(axis=1) / np.maximum(zscale, 1e-30)).max()
             report["max_rel_z"] = max(report.get("max_rel_z", 0.0), float(rel))
     return o
 
