@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q, "--format=csv,noheader",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -155,24 +155,30 @@ def _gen_inputs(cfg, threads=16):
     return kv, w
 
 
-def cpu_baseline(cfg, n_tokens=192, layer=0):
-    """The oracle as it stands, single-threaded, on evenly spaced tokens of one layer."""
+def cpu_baseline(cfg, budget_s=12.0, layer=0):
+    """The oracle as it stands, single-threaded, on non-reference tokens of one layer
+    taken in a fixed pseudo-random order until about `budget_s` seconds of CPU work."""
     import oracle
     kv = wl.layer_kv(cfg, layer)[0]
     w = wl.layer_weights(cfg, layer)
-    toks = np.linspace(1, cfg.T - 1, n_tokens).astype(np.int32)
-    toks = toks[toks % cfg.stride != cfg.first % cfg.stride]
+    non = np.nonzero((np.arange(cfg.T) - cfg.first) % cfg.stride != 0)[0]
+    order = np.random.default_rng(12345).permutation(non).astype(np.int32)
     kv64 = wl.stored_to_f64(kv, cfg.kv_dtype)
     ref_pos = oracle.schedule(cfg)
     refs64, _ = oracle.stored_refs(cfg, kv, ref_pos)
     w64 = oracle.weights_f64(cfg, w)
-    t0 = time.perf_counter()
-    oracle.compress_tokens(cfg, kv, w64, toks, kv64=kv64, refs64=refs64, ref_pos=ref_pos)
-    dt = time.perf_counter() - t0
-    return {"value": toks.size / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d non-reference tokens evenly spaced over layer %d of %s (T=%d), full write "
-                      "path per token (retrieval over the causal pool, mean, f_c twice, quantise), "
-                      "single-threaded fp64 C; %.1f s" % (toks.size, layer, cfg.name, cfg.T, dt)}
+    done, dt, batch = 0, 0.0, 16
+    while dt < budget_s and done < order.size:
+        toks = order[done:done + batch]
+        t0 = time.perf_counter()
+        oracle.compress_tokens(cfg, kv, w64, toks, kv64=kv64, refs64=refs64, ref_pos=ref_pos)
+        dt += time.perf_counter() - t0
+        done += toks.size
+        batch = min(512, batch * 2)
+    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d random non-reference tokens of layer %d of %s (T=%d), full write path per "
+                      "token (retrieval over the causal pool, mean, f_c twice, quantise), "
+                      "single-threaded fp64 C; %.1f s" % (done, layer, cfg.name, cfg.T, dt)}
 
 
 def run_reference(args, cfg):
@@ -370,16 +376,20 @@ def run_ours(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=WORKLOAD, choices=list(wl.CONFIGS))
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only this many layers (small profiling cases; 0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     cfg = wl.CONFIGS[args.config]
+    if args.layers > 0:
+        cfg = cfg.replace(L=args.layers)
     if cfg.gather_steps == 0:
         cfg = cfg.replace(gather_steps=1)
     if args.impl == "reference":

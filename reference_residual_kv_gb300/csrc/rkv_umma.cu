@@ -5,8 +5,9 @@
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 4 stages
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, bf16 -> fp32,
 //               into one of two 256-column TMEM accumulators
-//   warps 2..5  epilogue: one accumulator row (= one token or reference) per
-//               thread, read with tcgen05.ld while the next tile accumulates
+//   warps 2..9  epilogue: one accumulator row (= one token or reference) per
+//               thread and half of the columns per warp, read with tcgen05.ld
+//               while the next tile accumulates
 // The epilogue is what differs between the four uses:
 //   M_P    P1 | P2 = R [W_c1 | W_c2] for each stored reference (fp32 out)
 //   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kCand per row
@@ -31,7 +32,10 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMergeBytes = kBM * kCand * 8;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kMergeBytes;
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
 
 struct UmmaArgs {
@@ -87,8 +91,20 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float (&v
     *(uint4 *)dst = *(const uint4 *)o;
 }
 
+// named barrier of the epilogue warps only
+__device__ __forceinline__ void epi_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+// Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
+__device__ __forceinline__ float silu_fast(float u)
+{
+    return __fdividef(u, 1.0f + __expf(-u));
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
        const UmmaArgs a)
@@ -102,6 +118,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    volatile int *epi_abort = abort_flag + 1;
+    float2 *merge_buf = (float2 *)(tiles + kStages * kStageBytes + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -111,10 +129,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         }
         for (int b = 0; b < 2; ++b) {
             um::mbar_init(&tfull[b], 1);
-            um::mbar_init(&tempty[b], 128);
+            um::mbar_init(&tempty[b], 32 * kEpiWarps);
         }
         um::mbar_init(drain, 1);
         *abort_flag = 0;
+        *epi_abort = 0;
         um::fence_mbar_init();
     }
     if (warp == 1) {
@@ -224,12 +243,15 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                 // TMEM lanes [32q, 32q+32) belong to this warp
+        // 8 warps: warp w reads TMEM lanes [32q, 32q+32), q = w % 4 (hardware rule),
+        // and half h of the tile's columns.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t cnt = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             Item it;
             if (!item_get<MODE>(a, i, it)) continue;
             const int r = it.m * kBM + row;
@@ -244,19 +266,25 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 pool = in ? a.pool_size[r] : 0;
                 tile_pool = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1];
             }
-            int sl[4] = {-1, -1, -1, -1};
-            int kk = 0;
+            // S1: the token's references; unused slots point at slot 0 with weight 0 so
+            // that every gather load is issued unconditionally (more loads in flight)
+            int sl[4] = {0, 0, 0, 0};
+            float wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float inv_k = 0.0f;
             bool is_ref = true;
             if (MODE == M_S1 || MODE == M_S2) {
                 is_ref = in ? (a.ref_slot[r] >= 0) : true;
                 // a token equal to all its references has z = 0 exactly
                 if (MODE == M_S1 && in && !is_ref && a.copy_flag[(size_t)it.lb * a.T + r]) is_ref = true;
                 if (MODE == M_S1 && in && !is_ref) {
-                    int4 ix = a.ref_idx[(size_t)it.lb * a.T + r];
-                    sl[0] = ix.x; sl[1] = ix.y; sl[2] = ix.z; sl[3] = ix.w;
+                    const int4 ix = a.ref_idx[(size_t)it.lb * a.T + r];
+                    const int raw[4] = {ix.x, ix.y, ix.z, ix.w};
+                    int kk = 0;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (sl[j] >= 0) ++kk;
+                    for (int j = 0; j < 4; ++j) {
+                        if (raw[j] >= 0) { sl[j] = raw[j]; wt[j] = 1.0f; ++kk; }
+                    }
+                    inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
                 }
             }
 
@@ -269,7 +297,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 
                 if (MODE == M_P) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c0 = h * 64 + cc * 32;
                         float v1[32], v2[32];
                         um::tmem_ld32(tb + c0, v1);
                         um::tmem_ld32(tb + kBN / 2 + c0, v2);
@@ -287,9 +316,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 } else if (MODE == M_DIST) {
                     const float *rn = a.ref_sqnorm + (size_t)it.lb * a.n_ref;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    for (int c0 = h * (kBN / 2); c0 < (h + 1) * (kBN / 2); c0 += 32) {
                         const int s0 = n * kBN + c0;
-                        if (s0 >= tile_pool) break;          // uniform over the CTA
+                        if (s0 >= tile_pool) break;          // uniform over the warp
                         float v[32];
                         um::tmem_ld32(tb + c0, v);
                         const float rn_l = (s0 + lane < a.n_ref) ? rn[s0 + lane] : 0.0f;
@@ -298,8 +327,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const float rj = __shfl_sync(0xffffffffu, rn_l, j);
                             const float e = fmaf(-2.0f, v[j], rj);
                             if (s0 + j < pool && e < be[kCand - 1]) {
-                                // slots arrive in increasing order: strict < keeps the
-                                // lower slot ahead of an equal later one
+                                // this warp's slots arrive in increasing order: strict <
+                                // keeps the lower slot ahead of an equal later one
                                 float ce = e;
                                 int cs = s0 + j;
 #pragma unroll
@@ -315,9 +344,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 } else if (MODE == M_S1) {
-                    const size_t pbase = (size_t)it.lb * a.n_ref;
+                    const float *P1b = a.P1 + (size_t)it.lb * a.n_ref * a.d_ff;
+                    const float *P2b = a.P2 + (size_t)it.lb * a.n_ref * a.d_ff;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c0 = h * 64 + cc * 32;
                         float v1[32], v2[32];
                         um::tmem_ld32(tb + c0, v1);
                         um::tmem_ld32(tb + kBN / 2 + c0, v2);
@@ -325,31 +356,45 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (!in || f0 >= a.d_ff) continue;
                         __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
                         __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
+                        if (is_ref) {
+                            const float zero8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                            for (int s8 = 0; s8 < 4; ++s8) {
+                                store_bf16x8(hi + 8 * s8, zero8);
+                                store_bf16x8(lo + 8 * s8, zero8);
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int s8 = 0; s8 < 4; ++s8) {
+                            float4 x1[4][2], x2[4][2];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 *q1 = (const float4 *)(P1b + (size_t)sl[j] * a.d_ff + f0 + 8 * s8);
+                                const float4 *q2 = (const float4 *)(P2b + (size_t)sl[j] * a.d_ff + f0 + 8 * s8);
+                                x1[j][0] = __ldg(q1); x1[j][1] = __ldg(q1 + 1);
+                                x2[j][0] = __ldg(q2); x2[j][1] = __ldg(q2 + 1);
+                            }
                             float p1[8] = {0, 0, 0, 0, 0, 0, 0, 0}, p2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                if (sl[j] < 0) continue;
-                                const float4 *q1 = (const float4 *)(a.P1 + (pbase + sl[j]) * a.d_ff + f0 + 8 * s8);
-                                const float4 *q2 = (const float4 *)(a.P2 + (pbase + sl[j]) * a.d_ff + f0 + 8 * s8);
-                                const float4 x0 = __ldg(q1), x1 = __ldg(q1 + 1);
-                                const float4 y0 = __ldg(q2), y1 = __ldg(q2 + 1);
-                                p1[0] += x0.x; p1[1] += x0.y; p1[2] += x0.z; p1[3] += x0.w;
-                                p1[4] += x1.x; p1[5] += x1.y; p1[6] += x1.z; p1[7] += x1.w;
-                                p2[0] += y0.x; p2[1] += y0.y; p2[2] += y0.z; p2[3] += y0.w;
-                                p2[4] += y1.x; p2[5] += y1.y; p2[6] += y1.z; p2[7] += y1.w;
+                                const float wj = wt[j];
+                                p1[0] = fmaf(wj, x1[j][0].x, p1[0]); p1[1] = fmaf(wj, x1[j][0].y, p1[1]);
+                                p1[2] = fmaf(wj, x1[j][0].z, p1[2]); p1[3] = fmaf(wj, x1[j][0].w, p1[3]);
+                                p1[4] = fmaf(wj, x1[j][1].x, p1[4]); p1[5] = fmaf(wj, x1[j][1].y, p1[5]);
+                                p1[6] = fmaf(wj, x1[j][1].z, p1[6]); p1[7] = fmaf(wj, x1[j][1].w, p1[7]);
+                                p2[0] = fmaf(wj, x2[j][0].x, p2[0]); p2[1] = fmaf(wj, x2[j][0].y, p2[1]);
+                                p2[2] = fmaf(wj, x2[j][0].z, p2[2]); p2[3] = fmaf(wj, x2[j][0].w, p2[3]);
+                                p2[4] = fmaf(wj, x2[j][1].x, p2[4]); p2[5] = fmaf(wj, x2[j][1].y, p2[5]);
+                                p2[6] = fmaf(wj, x2[j][1].z, p2[6]); p2[7] = fmaf(wj, x2[j][1].w, p2[7]);
                             }
-                            float dh[8], h8[8], l8[8];
+                            float h8[8], l8[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                float m1 = p1[j], m2 = p2[j];
-                                if (kk > 0) { m1 = __fdiv_rn(m1, (float)kk); m2 = __fdiv_rn(m2, (float)kk); }
-                                const float x1v = v1[8 * s8 + j], x2v = v2[8 * s8 + j];
-                                dh[j] = is_ref ? 0.0f : silu(x1v) * x2v - silu(m1) * m2;
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh[j]);
-                                h8[j] = __bfloat162float(hb);
-                                l8[j] = dh[j] - h8[j];
+                                const float m1 = p1[j] * inv_k, m2 = p2[j] * inv_k;
+                                const float dh = silu_fast(v1[8 * s8 + j]) * v2[8 * s8 + j] - silu_fast(m1) * m2;
+                                h8[j] = __bfloat162float(__float2bfloat16_rn(dh));
+                                l8[j] = dh - h8[j];
                             }
                             store_bf16x8(hi + 8 * s8, h8);
                             store_bf16x8(lo + 8 * s8, l8);
@@ -357,7 +402,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                 } else {  // M_S2
 #pragma unroll 1
-                    for (int g8 = 0; g8 < kBN / 32; ++g8) {
+                    for (int g8 = h * 4; g8 < h * 4 + 4; ++g8) {
                         const int c0 = n * kBN + g8 * 32;
                         if (c0 >= a.d_c) break;              // uniform
                         float v[32];
@@ -388,12 +433,46 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 um::mbar_arrive(&tempty[buf]);
                 ++cnt;
             }
-            if (MODE == M_DIST && ok && in) {
-                float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand);
+            if (MODE == M_DIST) {
+                // merge the two column halves' lists of each row.  Every epilogue warp
+                // passes the three barriers once per item, also when aborting; the
+                // decision to stop comes from a flag that only epilogue warps write,
+                // and only before the first barrier, so all of them read one value.
+                if (!ok) *epi_abort = 1;
+                epi_bar();
+                const bool stop = *epi_abort != 0;
+                if (!stop && h == 1) {
 #pragma unroll
-                for (int j = 0; j < kCand / 2; ++j)
-                    cp[j] = make_float4(be[2 * j], __int_as_float(bs[2 * j]), be[2 * j + 1],
-                                        __int_as_float(bs[2 * j + 1]));
+                    for (int j = 0; j < kCand; ++j) merge_buf[row * kCand + j] = make_float2(be[j], __int_as_float(bs[j]));
+                }
+                epi_bar();
+                if (!stop && h == 0 && in) {
+#pragma unroll
+                    for (int j = 0; j < kCand; ++j) {
+                        const float2 o = merge_buf[row * kCand + j];
+                        float ce = o.x;
+                        int cs = __float_as_int(o.y);
+                        if (cs < 0) break;
+#pragma unroll
+                        for (int qq = 0; qq < kCand; ++qq) {
+                            const bool lt = ce < be[qq] || (ce == be[qq] && (unsigned)cs < (unsigned)bs[qq]);
+                            const float te = lt ? be[qq] : ce;
+                            const int ts = lt ? bs[qq] : cs;
+                            if (lt) { be[qq] = ce; bs[qq] = cs; }
+                            ce = te;
+                            cs = ts;
+                        }
+                    }
+                    float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand);
+#pragma unroll
+                    for (int j = 0; j < kCand / 2; ++j)
+                        cp[j] = make_float4(be[2 * j], __int_as_float(bs[2 * j]), be[2 * j + 1],
+                                            __int_as_float(bs[2 * j + 1]));
+                }
+                epi_bar();
+                if (stop) { ok = false; break; }
+            } else if (!ok) {
+                break;
             }
         }
         if (!ok) {
@@ -460,7 +539,7 @@ static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUten
     static const char *names[4] = {"umma_ref_proj", "umma_distance_topk", "umma_swiglu_diff",
                                    "umma_z_quant"};
     ProfScope prof(names[MODE], s);
-    k_umma<MODE><<<grid, 192, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+    k_umma<MODE><<<grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
     return cudaGetLastError();
 }
 
