@@ -57,28 +57,37 @@ struct UmmaArgs {
 
 struct Item { int lb, m, n0, n1, chunk; };
 
-template <int MODE>
+// A cluster of C CTAs works on C consecutive token tiles against the same B tiles
+// (weights or references), each CTA loading 1/C of every B tile and multicasting it
+// to all C.
+template <int C>
+__device__ __forceinline__ int n_groups(const UmmaArgs &a) { return (a.n_mtiles + C - 1) / C; }
+
+template <int MODE, int C>
 __device__ __forceinline__ int item_count(const UmmaArgs &a)
 {
-    return a.LB * a.n_mtiles * (MODE == M_DIST ? a.max_chunks : a.n_ntiles);
+    return a.LB * n_groups<C>(a) * (MODE == M_DIST ? a.max_chunks : a.n_ntiles);
 }
 
-// Work item i -> (lb, token tile, N-tile range).  Distance items visit the late
-// (largest-pool) token tiles first.
-template <int MODE>
-__device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, Item &it)
+// Work item i -> (lb, this CTA's token tile, N-tile range), identical N range and K
+// loop for all CTAs of the cluster.  Distance items visit the late (largest-pool)
+// token tiles first; a group's N range is that of its last tile.
+template <int MODE, int C>
+__device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, int rank, Item &it)
 {
+    const int ng = n_groups<C>(a);
     if (MODE == M_DIST) {
         const int chunk = i % a.max_chunks, r = i / a.max_chunks;
-        const int lb = r % a.LB, m = a.n_mtiles - 1 - r / a.LB;
-        const int nt = dist_ntiles(a.pool_size, a.T, m);
-        it.lb = lb; it.m = m; it.chunk = chunk;
+        const int lb = r % a.LB, g = ng - 1 - r / a.LB;
+        const int last = min(a.n_mtiles - 1, g * C + C - 1);
+        const int nt = dist_ntiles(a.pool_size, a.T, last);
+        it.lb = lb; it.m = g * C + rank; it.chunk = chunk;
         it.n0 = chunk * kDistChunk;
         it.n1 = min(nt, it.n0 + kDistChunk);
         return it.n0 < it.n1;
     }
     const int n = i % a.n_ntiles, r = i / a.n_ntiles;
-    it.lb = r % a.LB; it.m = r / a.LB; it.chunk = 0;
+    it.lb = r % a.LB; it.m = (r / a.LB) * C + rank; it.chunk = 0;
     it.n0 = n; it.n1 = n + 1;
     return true;
 }
@@ -103,7 +112,7 @@ __device__ __forceinline__ float silu_fast(float u)
     return __fdividef(u, 1.0f + __expf(-u));
 }
 
-template <int MODE>
+template <int MODE, int C>
 __global__ void __launch_bounds__(kThreads, 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -125,7 +134,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             um::mbar_init(&full[s], 1);
-            um::mbar_init(&empty[s], 1);
+            um::mbar_init(&empty[s], C);          // one commit from every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             um::mbar_init(&tfull[b], 1);
@@ -141,10 +150,15 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         um::tmem_relinquish();
     }
     um::tc_fence_before();
-    __syncthreads();
+    if (C > 1) um::cluster_sync();   // peers multicast into our stages only after our init
+    else __syncthreads();
     um::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = item_count<MODE>(a);
+    const int n_items = item_count<MODE, C>(a);
+    const int rank = C > 1 ? (int)um::cluster_rank() : 0;
+    const int cid = blockIdx.x / C, ncl = gridDim.x / C;
+    constexpr uint16_t kMask = (uint16_t)((1u << C) - 1u);
+    constexpr int kSlice = kBN / C;                // B rows each CTA loads
     const int k_iters = a.k_chunks * a.a_sources;
 
     if (warp == 0) {
@@ -160,9 +174,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             bool used[kStages];
             for (int s = 0; s < kStages; ++s) { used[s] = false; last_ph[s] = 0; }
             bool ok = true;
-            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            for (int i = cid; i < n_items && ok; i += ncl) {
                 Item it;
-                if (!item_get<MODE>(a, i, it)) continue;
+                if (!item_get<MODE, C>(a, i, rank, it)) continue;
                 const int bz = a.b_per_layer ? it.lb / a.B : it.lb;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     for (int kc = 0; kc < k_iters; ++kc) {
@@ -176,11 +190,24 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const int src = kc / a.k_chunks;
                         const int kx = (kc - src * a.k_chunks) * kBK;
                         um::tma_load_3d(sa, src ? &tmA1 : &tmA0, &full[stage], kx, it.m * kBM, it.lb);
-                        if (a.b_split) {
-                            um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * (kBN / 2), bz);
-                            um::tma_load_3d(sb + kBBytes / 2, &tmB1, &full[stage], kx, n * (kBN / 2), bz);
+                        if (C == 1) {
+                            if (a.b_split) {
+                                um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * (kBN / 2), bz);
+                                um::tma_load_3d(sb + kBBytes / 2, &tmB1, &full[stage], kx, n * (kBN / 2), bz);
+                            } else {
+                                um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * kBN, bz);
+                            }
                         } else {
-                            um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * kBN, bz);
+                            // this CTA's slice of the B tile, into every CTA of the cluster;
+                            // split B: slices [0, C/2) from tmB0, [C/2, C) from tmB1
+                            uint8_t *dst = sb + rank * kSlice * (kBK * 2);
+                            if (a.b_split) {
+                                const int hs = C / 2;
+                                const int yrow = n * (kBN / 2) + (rank % hs) * kSlice;
+                                um::tma_load_3d_mc(dst, rank < hs ? &tmB0 : &tmB1, &full[stage], kx, yrow, bz, kMask);
+                            } else {
+                                um::tma_load_3d_mc(dst, &tmB0, &full[stage], kx, n * kBN + rank * kSlice, bz, kMask);
+                            }
                         }
                         used[stage] = true;
                         last_ph[stage] = ph;
@@ -202,9 +229,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             int stage = 0;
             uint32_t ph = 0, cnt = 0;
             bool ok = true;
-            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            for (int i = cid; i < n_items && ok; i += ncl) {
                 Item it;
-                if (!item_get<MODE>(a, i, it)) continue;
+                if (!item_get<MODE, C>(a, i, rank, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
                     if (*abort_flag || !um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles)) {
@@ -225,7 +252,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
                             um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
-                        um::mma_commit(&empty[stage]);
+                        if (C > 1) um::mma_commit_mc(&empty[stage], kMask);
+                        else um::mma_commit(&empty[stage]);
                         if (++stage == kStages) { stage = 0; ph ^= 1u; }
                     }
                     if (!ok) break;
@@ -251,9 +279,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t cnt = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+        for (int i = cid; i < n_items; i += ncl) {
             Item it;
-            if (!item_get<MODE>(a, i, it)) continue;
+            if (!item_get<MODE, C>(a, i, rank, it)) continue;
             const int r = it.m * kBM + row;
             const bool in = r < a.rows;
 
@@ -482,7 +510,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     }
 
     um::tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or signal its barriers
+    if (C > 1) um::cluster_sync();
+    else __syncthreads();
     if (warp == 1) {
         um::tc_fence_after();
         um::tmem_dealloc(tmem_base, 512);
@@ -520,26 +550,49 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// Clusters of kCluster CTAs share every B tile through TMA multicast.
+constexpr int kCluster = 2;
+
 template <int MODE>
 static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
                        const CUtensorMap &b1, const UmmaArgs &args, cudaStream_t s)
 {
+    constexpr int C = kCluster;
+    auto kern = k_umma<MODE, C>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_umma<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const long long items =
-        (long long)args.LB * args.n_mtiles * (MODE == M_DIST ? args.max_chunks : args.n_ntiles);
+    const long long groups = (args.n_mtiles + C - 1) / C;
+    const long long items = (long long)args.LB * groups * (MODE == M_DIST ? args.max_chunks : args.n_ntiles);
     if (items <= 0) return cudaSuccess;
-    const int sms = device_sm_count();
-    const int grid = (int)(items < sms ? items : sms);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    static int max_clusters = 0;
+    if (max_clusters == 0) {
+        cfg.gridDim = dim3(C * 64, 1, 1);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, (void *)kern, &cfg);
+        if (e != cudaSuccess || max_clusters <= 0) max_clusters = device_sm_count() / C;
+    }
+    const long long nc = items < max_clusters ? items : max_clusters;
+    cfg.gridDim = dim3((unsigned)(nc * C), 1, 1);
     static const char *names[4] = {"umma_ref_proj", "umma_distance_topk", "umma_swiglu_diff",
                                    "umma_z_quant"};
     ProfScope prof(names[MODE], s);
-    k_umma<MODE><<<grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -570,16 +623,20 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     const int kw = (g.W + kBK - 1) / kBK;
 
     CUtensorMap mX, mW1, mW2, mW3, mHi, mLo, mRa, mRb;
-    if (!make_map(&mX, kv, g.W, g.T, g.LB, kBM) || !make_map(&mW1, W1t, g.W, g.d_ff, g.L, kBN / 2) ||
-        !make_map(&mW2, W2t, g.W, g.d_ff, g.L, kBN / 2) ||
-        !make_map(&mW3, W3t, g.d_ff, g.d_c, g.L, kBN) ||
+    // B maps load one cluster slice per box: kBN / kCluster rows
+    constexpr int kSliceRows = kBN / kCluster;
+    static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster of 1, 2 or 4");
+    const int split_rows = kCluster == 1 ? kBN / 2 : kSliceRows;
+    if (!make_map(&mX, kv, g.W, g.T, g.LB, kBM) || !make_map(&mW1, W1t, g.W, g.d_ff, g.L, split_rows) ||
+        !make_map(&mW2, W2t, g.W, g.d_ff, g.L, split_rows) ||
+        !make_map(&mW3, W3t, g.d_ff, g.d_c, g.L, kSliceRows) ||
         !make_map(&mHi, dh_hi, g.d_ff, g.T, g.LB, kBM) ||
         !make_map(&mLo, dh_lo, g.d_ff, g.T, g.LB, kBM))
         return cudaErrorInvalidValue;
 
     if (g.n_ref > 0) {
         if (!make_map(&mRa, ref_mma, g.W, g.n_ref, g.LB, kBM) ||
-            !make_map(&mRb, ref_mma, g.W, g.n_ref, g.LB, kBN))
+            !make_map(&mRb, ref_mma, g.W, g.n_ref, g.LB, kSliceRows))
             return cudaErrorInvalidValue;
         // P1 | P2 for every reference
         UmmaArgs p = a;

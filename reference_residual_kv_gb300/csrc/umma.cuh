@@ -73,6 +73,34 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// Multicast tile load: the box lands at the same shared-memory offset in every CTA of
+// the cluster named in `mask`, and each of them gets the complete_tx on its own
+// mbarrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
+                                               int x, int y, int z, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+// ---- clusters ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA in the cluster; release/acquire orders shared memory.
+__device__ __forceinline__ void cluster_sync()
+{
+    __syncwarp();   // .aligned: every warp arrives converged
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- TMEM / tcgen05 --------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
 {
@@ -141,6 +169,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// Same, arriving on the mbarrier at `bar`'s offset in every CTA named in `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 
