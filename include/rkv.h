@@ -148,6 +148,28 @@ rkv_status rkv_gather_dequant(const rkv_params *p, const rkv_ref_pool *pool,
                               void *out_z, void *out_mean, int32_t out_dtype,
                               int32_t *dev_status, void *stream);
 
+/* rkv_compress without a workspace argument: for callers that cannot allocate
+ * device memory at the call site -- code running while a CUDA graph is captured
+ * (cudaMalloc is not allowed there), runtimes whose device memory belongs to an
+ * arena the caller cannot reach, serving loops that must not allocate after
+ * start-up.  The paper has no counterpart; this is an interface convenience.
+ * Same arguments, semantics and results as rkv_compress, except that the scratch
+ * is a fixed 64 MiB array inside the library's device image (a device holds it
+ * until the process exits; with lazy module loading it is reserved when this entry
+ * point is first used on that device).  Problems whose rkv_query_sizes()
+ * workspace exceeds 64 MiB return RKV_ERR_WORKSPACE and launch nothing (one
+ * Llama-3.1-8B-shape layer of 8192 tokens fits).  It calls no cudaMalloc/cudaFree
+ * and no allocating library routine.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the one array and nothing in it needs to
+ * start at zero (every byte read is written earlier in the same call), but calls
+ * that overlap on the GPU -- on different streams, or from several host threads --
+ * race on it: serialise them.                                                      */
+rkv_status rkv_compress_noalloc(const rkv_params *p, const void *kv, const rkv_ref_pool *pool,
+                                const void *W1t, const void *W2t, const void *W3t,
+                                const rkv_cache *cache, float *z_out, int32_t *dev_status,
+                                void *stream);
+
 /* Diagnostics: per-kernel device time.  rkv_profile_enable(1) clears the record
  * and brackets every later kernel launch of the library with two CUDA events on
  * the launch stream; rkv_profile_enable(0) stops recording.  rkv_profile_collect

@@ -17,7 +17,8 @@ RKV_F32, RKV_BF16, RKV_FP8_E4M3 = 0, 1, 2
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_ALIGNMENT = 0, 1, 2, 3
 RKV_ERR_CUDA, RKV_ERR_INDEX, RKV_ERR_DEVICE_TIMEOUT, RKV_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("rkv_n_ref", "rkv_query_sizes", "rkv_build_ref_pool", "rkv_compress",
-            "rkv_gather_dequant", "rkv_profile_enable", "rkv_profile_collect", "rkv_status_string")
+            "rkv_gather_dequant", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
+            "rkv_status_string")
 _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 
 
@@ -65,6 +66,9 @@ def lib():
         L.rkv_compress.argtypes = [P, V, ctypes.POINTER(rkv_ref_pool), V, V, V,
                                    ctypes.POINTER(rkv_cache), V, ctypes.c_size_t, V, V, V]
         L.rkv_compress.restype = I32
+        L.rkv_compress_noalloc.argtypes = [P, V, ctypes.POINTER(rkv_ref_pool), V, V, V,
+                                           ctypes.POINTER(rkv_cache), V, V, V]
+        L.rkv_compress_noalloc.restype = I32
         L.rkv_gather_dequant.argtypes = [P, ctypes.POINTER(rkv_ref_pool), ctypes.POINTER(rkv_cache),
                                          V, I32, V, V, I32, V, V]
         L.rkv_gather_dequant.restype = I32
@@ -138,6 +142,17 @@ def rkv_compress(p: rkv_params, kv, pool: rkv_ref_pool, W1t, W2t, W3t, cache: rk
                             _ptr(z_out), _ptr(dev_status), _stream(stream))
     if st:
         raise RkvError(st, "rkv_compress")
+
+
+def rkv_compress_noalloc(p: rkv_params, kv, pool: rkv_ref_pool, W1t, W2t, W3t, cache: rkv_cache,
+                         z_out, dev_status, stream=None) -> None:
+    """rkv_compress with the library's built-in 64 MiB scratch instead of a workspace
+    (for callers that cannot allocate device memory at the call)."""
+    st = lib().rkv_compress_noalloc(ctypes.byref(p), _ptr(kv), ctypes.byref(pool), _ptr(W1t),
+                                    _ptr(W2t), _ptr(W3t), ctypes.byref(cache), _ptr(z_out),
+                                    _ptr(dev_status), _stream(stream))
+    if st:
+        raise RkvError(st, "rkv_compress_noalloc")
 
 
 def rkv_gather_dequant(p: rkv_params, pool: rkv_ref_pool, cache: rkv_cache, sel, n_sel: int,
