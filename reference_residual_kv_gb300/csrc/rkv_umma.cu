@@ -70,15 +70,18 @@ __device__ __forceinline__ int item_count(const UmmaArgs &a)
 }
 
 // Work item i -> (lb, this CTA's token tile, N-tile range), identical N range and K
-// loop for all CTAs of the cluster.  Distance items visit the late (largest-pool)
-// token tiles first; a group's N range is that of its last tile.
+// loop for all CTAs of the cluster.  The (layer, sequence) index is the slowest, so
+// the CTAs in flight share one layer's weights, references and projections in L2;
+// the N tile is the fastest, so neighbouring CTAs reuse the same token rows.
+// Distance items visit the late (largest-pool) token tiles first; a group's N range
+// is that of its last tile.
 template <int MODE, int C>
 __device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, int rank, Item &it)
 {
     const int ng = n_groups<C>(a);
     if (MODE == M_DIST) {
         const int chunk = i % a.max_chunks, r = i / a.max_chunks;
-        const int lb = r % a.LB, g = ng - 1 - r / a.LB;
+        const int g = ng - 1 - r % ng, lb = r / ng;
         const int last = min(a.n_mtiles - 1, g * C + C - 1);
         const int nt = dist_ntiles(a.pool_size, a.T, last);
         it.lb = lb; it.m = g * C + rank; it.chunk = chunk;
@@ -87,7 +90,7 @@ __device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, int rank, Ite
         return it.n0 < it.n1;
     }
     const int n = i % a.n_ntiles, r = i / a.n_ntiles;
-    it.lb = r % a.LB; it.m = (r / a.LB) * C + rank; it.chunk = 0;
+    it.m = (r % ng) * C + rank; it.lb = r / ng; it.chunk = 0;
     it.n0 = n; it.n1 = n + 1;
     return true;
 }
