@@ -42,8 +42,9 @@ Workspace workspace_layout(const Geometry &g)
     const size_t LB = (size_t)g.LB, T = (size_t)g.T, R = (size_t)g.n_ref;
     const bool tc = g.kv_dtype == RKV_BF16;
     w.ref_mma = take(g.ref_dtype == RKV_FP8_E4M3 ? LB * R * g.W * 2 : 0);
-    w.P1 = take(LB * R * g.d_ff * 4);
-    w.P2 = take(LB * R * g.d_ff * 4);
+    // one extra all-zero row after the last reference's row (padding for unused slots)
+    w.P1 = take((LB * R + 1) * g.d_ff * 4);
+    w.P2 = take((LB * R + 1) * g.d_ff * 4);
     w.rn_max = take(LB * 4);
     w.cand = take(tc ? LB * T * g.max_chunks * kCand * 8 : 0);
     w.copy_flag = take(LB * T);
@@ -181,6 +182,8 @@ rkv_status rkv_compress(const rkv_params *p, const void *kv, const rkv_ref_pool 
     Geometry g = make_geometry(p);
     // tensor-core path: epilogues work on 32-column slices of d_ff
     if (g.kv_dtype == RKV_BF16 && g.d_ff % 32 != 0) return RKV_ERR_UNSUPPORTED;
+    // projection-row offsets are 32-bit in the encoder
+    if (((long long)g.LB * g.n_ref + 1) * g.d_ff >= (1LL << 31)) return RKV_ERR_UNSUPPORTED;
     Workspace wl = workspace_layout(g);
     if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return RKV_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255u) != 0) return RKV_ERR_ALIGNMENT;

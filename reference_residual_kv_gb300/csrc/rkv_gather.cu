@@ -115,6 +115,7 @@ k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int 
 
     // mean of the stored references, summed in ascending slot order, then / k
     const RefT *rbase = ref_vec + (size_t)lb * n_ref * W;
+#pragma unroll 2
     for (int c = lane * 8; c < W; c += 256) {
         float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll

@@ -62,7 +62,7 @@ cudaError_t launch_build_schedule(const Geometry &g, const rkv_ref_pool *pool, c
 cudaError_t launch_build_refs(const Geometry &g, const void *kv, const rkv_ref_pool *pool,
                               cudaStream_t s);
 cudaError_t launch_prep_refs(const Geometry &g, const rkv_ref_pool *pool, void *ref_mma,
-                             float *rn_max, cudaStream_t s);
+                             float *rn_max, float *zero_row1, float *zero_row2, cudaStream_t s);
 cudaError_t launch_gather(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
                           const int32_t *sel, int n_sel, void *out_z, void *out_mean,
                           int out_dtype, int32_t *status, cudaStream_t s);

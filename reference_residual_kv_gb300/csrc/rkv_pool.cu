@@ -129,11 +129,16 @@ __global__ void k_decode_fp8_refs(const uint8_t *__restrict__ src, __nv_bfloat16
     }
 }
 
-// rn_max[lb] = max_m ref_sqnorm[lb][m]  (scale of the distance-expansion error bound)
-__global__ void k_rn_max(const float *__restrict__ rn, float *__restrict__ out, int n_ref)
+// rn_max[lb] = max_m ref_sqnorm[lb][m]  (scale of the distance-expansion error bound);
+// block 0 also clears the all-zero projection rows (if given)
+__global__ void k_rn_max(const float *__restrict__ rn, float *__restrict__ out, int n_ref,
+                         float *__restrict__ z1, float *__restrict__ z2, int d_ff)
 {
     __shared__ float sm[32];
     const int lb = blockIdx.x;
+    if (lb == 0 && z1) {
+        for (int i = threadIdx.x; i < d_ff; i += blockDim.x) { z1[i] = 0.0f; z2[i] = 0.0f; }
+    }
     float v = 0.0f;
     for (int m = threadIdx.x; m < n_ref; m += blockDim.x) v = fmaxf(v, rn[(size_t)lb * n_ref + m]);
 #pragma unroll
@@ -149,9 +154,14 @@ __global__ void k_rn_max(const float *__restrict__ rn, float *__restrict__ out, 
 }
 
 cudaError_t launch_prep_refs(const Geometry &g, const rkv_ref_pool *pool, void *ref_mma,
-                             float *rn_max, cudaStream_t s)
+                             float *rn_max, float *zero_row1, float *zero_row2, cudaStream_t s)
 {
-    if (g.n_ref == 0) return cudaMemsetAsync(rn_max, 0, sizeof(float) * g.LB, s);
+    if (g.n_ref == 0) {
+        cudaError_t e = cudaMemsetAsync(rn_max, 0, sizeof(float) * g.LB, s);
+        if (e == cudaSuccess && zero_row1) e = cudaMemsetAsync(zero_row1, 0, sizeof(float) * g.d_ff, s);
+        if (e == cudaSuccess && zero_row2) e = cudaMemsetAsync(zero_row2, 0, sizeof(float) * g.d_ff, s);
+        return e;
+    }
     if (g.ref_dtype == RKV_FP8_E4M3) {
         long long n8 = (long long)g.LB * g.n_ref * g.W / 8;
         int blocks = (int)((n8 + 255) / 256);
@@ -161,7 +171,7 @@ cudaError_t launch_prep_refs(const Geometry &g, const rkv_ref_pool *pool, void *
                                                  (__nv_bfloat16 *)ref_mma, n8);
     }
     ProfScope prof("ref_norm_max", s);
-    k_rn_max<<<g.LB, 256, 0, s>>>(pool->ref_sqnorm, rn_max, g.n_ref);
+    k_rn_max<<<g.LB, 256, 0, s>>>(pool->ref_sqnorm, rn_max, g.n_ref, zero_row1, zero_row2, g.d_ff);
     return cudaGetLastError();
 }
 

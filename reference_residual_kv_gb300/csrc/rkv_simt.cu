@@ -197,7 +197,7 @@ cudaError_t launch_simt_compress(const Geometry &g, const void *kv, const rkv_re
     float *P1 = (float *)(ws + wl.P1), *P2 = (float *)(ws + wl.P2);
     float *rn_max = (float *)(ws + wl.rn_max);
     float *dh = (float *)(ws + wl.dh32), *z = (float *)(ws + wl.z32);
-    if ((e = launch_prep_refs(g, pool, nullptr, rn_max, s)) != cudaSuccess) return e;
+    if ((e = launch_prep_refs(g, pool, nullptr, rn_max, nullptr, nullptr, s)) != cudaSuccess) return e;
     const float *X = (const float *)kv;
     if (g.n_ref > 0) {
         dim3 grid((g.d_ff + 31) / 32, (g.n_ref + 63) / 64, g.LB);

@@ -72,14 +72,25 @@ __device__ __forceinline__ float warp_sqdist(const T *x, const T *r, int W, int 
 template <typename T>
 __device__ __forceinline__ float warp_sqnorm(const T *x, int W, int lane)
 {
-    float acc = 0.0f;
-    for (int c = lane * 8; c < W; c += 256) {
+    // four independent 8-element loads in flight per lane
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int c = lane * 8;
+    for (; c + 3 * 256 < W; c += 4 * 256) {
+        float a[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) Vec8<T>::load(x + c + u * 256, a[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[u] = fmaf(a[u][j], a[u][j], acc[u]);
+    }
+    for (; c < W; c += 256) {
         float a[8];
         Vec8<T>::load(x + c, a);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc = fmaf(a[j], a[j], acc);
+        for (int j = 0; j < 8; ++j) acc[0] = fmaf(a[j], a[j], acc[0]);
     }
-    return warp_tree_sum(acc);
+    return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
 
 __device__ __forceinline__ bool key_less(float ea, int sa, float eb, int sb)

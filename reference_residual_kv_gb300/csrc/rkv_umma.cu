@@ -37,6 +37,14 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMergeBytes = kBM * kCand * 8;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kMergeBytes;
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
+// projections run transposed: D[f][t] = W[f][:] . X[t][:], two 128x128 MMAs per step
+constexpr uint32_t kIdescT = um::idesc_bf16_f32(kBM, kBN / 2);
+
+// M_P and M_S1 put the weights on the MMA's M side (TMEM lane = d_ff column f) and
+// the tokens (or references) on N (TMEM column = token), so that the epilogue's
+// per-token gathers of reference projections and its stores are coalesced across
+// the 32 lanes of a warp (consecutive f).
+template <int MODE> struct Transposed { static constexpr bool value = MODE == M_P || MODE == M_S1; };
 
 struct UmmaArgs {
     int LB, B, T, rows;   // rows: A-operand rows per lb (T, or n_ref for M_P)
@@ -252,9 +260,19 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const uint32_t sa = um::smem_u32(tiles + stage * kStageBytes);
                         const uint64_t ad = um::sdesc_sw128(sa);
                         const uint64_t bd = um::sdesc_sw128(sa + kABytes);
+                        if (Transposed<MODE>::value) {
+                            // stage = [token tile | W1 tile | W2 tile]: D1 = W1 X^T, D2 = W2 X^T
+                            const uint64_t w1 = bd, w2 = um::sdesc_sw128(sa + kABytes + kBBytes / 2);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                            for (int k = 0; k < kBK / 16; ++k) {
+                                um::mma_bf16(d_tmem, w1 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
+                                um::mma_bf16(d_tmem + kBN / 2, w2 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; ++k)
+                                um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                        }
                         if (C > 1) um::mma_commit_mc(&empty[stage], kMask);
                         else um::mma_commit(&empty[stage]);
                         if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -297,27 +315,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 pool = in ? a.pool_size[r] : 0;
                 tile_pool = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1];
             }
-            // S1: the token's references; unused slots point at slot 0 with weight 0 so
-            // that every gather load is issued unconditionally (more loads in flight)
-            int sl[4] = {0, 0, 0, 0};
-            float wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            float inv_k = 0.0f;
             bool is_ref = true;
-            if (MODE == M_S1 || MODE == M_S2) {
-                is_ref = in ? (a.ref_slot[r] >= 0) : true;
-                // a token equal to all its references has z = 0 exactly
-                if (MODE == M_S1 && in && !is_ref && a.copy_flag[(size_t)it.lb * a.T + r]) is_ref = true;
-                if (MODE == M_S1 && in && !is_ref) {
-                    const int4 ix = a.ref_idx[(size_t)it.lb * a.T + r];
-                    const int raw[4] = {ix.x, ix.y, ix.z, ix.w};
-                    int kk = 0;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (raw[j] >= 0) { sl[j] = raw[j]; wt[j] = 1.0f; ++kk; }
-                    }
-                    inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
-                }
-            }
+            if (MODE == M_S2) is_ref = in ? (a.ref_slot[r] >= 0) : true;
 
             for (int n = it.n0; n < it.n1; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
@@ -327,20 +326,24 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const uint32_t tb = tl + buf * kBN;
 
                 if (MODE == M_P) {
+                    // lane = d_ff column f, TMEM column = reference slot
+                    const int f = n * (kBN / 2) + q * 32 + lane;
 #pragma unroll 1
                     for (int cc = 0; cc < 2; ++cc) {
                         const int c0 = h * 64 + cc * 32;
                         float v1[32], v2[32];
                         um::tmem_ld32(tb + c0, v1);
                         um::tmem_ld32(tb + kBN / 2 + c0, v2);
-                        const int f0 = n * (kBN / 2) + c0;
-                        if (in && f0 < a.d_ff) {
-                            float4 *p1 = (float4 *)(a.P1 + ((size_t)it.lb * a.n_ref + r) * a.d_ff + f0);
-                            float4 *p2 = (float4 *)(a.P2 + ((size_t)it.lb * a.n_ref + r) * a.d_ff + f0);
+                        const int r0 = it.m * kBM + c0;
+                        if (f < a.d_ff) {
+                            float *p1 = a.P1 + ((size_t)it.lb * a.n_ref + r0) * a.d_ff + f;
+                            float *p2 = a.P2 + ((size_t)it.lb * a.n_ref + r0) * a.d_ff + f;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                p1[j] = make_float4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
-                                p2[j] = make_float4(v2[4 * j], v2[4 * j + 1], v2[4 * j + 2], v2[4 * j + 3]);
+                            for (int j = 0; j < 32; ++j) {
+                                if (r0 + j < a.rows) {
+                                    p1[(size_t)j * a.d_ff] = v1[j];
+                                    p2[(size_t)j * a.d_ff] = v2[j];
+                                }
                             }
                         }
                     }
@@ -375,60 +378,72 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 } else if (MODE == M_S1) {
-                    const float *P1b = a.P1 + (size_t)it.lb * a.n_ref * a.d_ff;
-                    const float *P2b = a.P2 + (size_t)it.lb * a.n_ref * a.d_ff;
+                    // lane = d_ff column f, TMEM column = token.  For each token the
+                    // warp reads its references' projection rows as 128-byte lines.
+                    // Lane j first prepares token j's 32-bit row offsets (unused slots
+                    // point at the all-zero row), 1/k and a live flag in shared memory.
+                    const int f = n * (kBN / 2) + q * 32 + lane;
+                    const bool fok = f < a.d_ff;
+                    const float *P1f = a.P1 + (fok ? f : 0);
+                    const float *P2f = a.P2 + (fok ? f : 0);
+                    int4 *info = (int4 *)merge_buf + (warp - 2) * 64;   // 32 tokens x 2 int4
+                    const int zoff = a.LB * a.n_ref * a.d_ff;
+                    const int lboff = it.lb * a.n_ref;
 #pragma unroll 1
                     for (int cc = 0; cc < 2; ++cc) {
                         const int c0 = h * 64 + cc * 32;
                         float v1[32], v2[32];
                         um::tmem_ld32(tb + c0, v1);
                         um::tmem_ld32(tb + kBN / 2 + c0, v2);
-                        const int f0 = n * (kBN / 2) + c0;
-                        if (!in || f0 >= a.d_ff) continue;
-                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
-                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + r) * a.d_ff + f0;
-                        if (is_ref) {
-                            const float zero8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-                            for (int s8 = 0; s8 < 4; ++s8) {
-                                store_bf16x8(hi + 8 * s8, zero8);
-                                store_bf16x8(lo + 8 * s8, zero8);
+                        const int t0 = it.m * kBM + c0;
+                        {
+                            const int tj = t0 + lane;
+                            int4 o = make_int4(zoff, zoff, zoff, zoff);
+                            float inv_k = 0.0f, live = 0.0f;
+                            if (tj < a.rows && a.ref_slot[tj] < 0 && !a.copy_flag[(size_t)it.lb * a.T + tj]) {
+                                const int4 ix = a.ref_idx[(size_t)it.lb * a.T + tj];
+                                int kk = 0;
+                                if (ix.x >= 0) { o.x = (lboff + ix.x) * a.d_ff; ++kk; }
+                                if (ix.y >= 0) { o.y = (lboff + ix.y) * a.d_ff; ++kk; }
+                                if (ix.z >= 0) { o.z = (lboff + ix.z) * a.d_ff; ++kk; }
+                                if (ix.w >= 0) { o.w = (lboff + ix.w) * a.d_ff; ++kk; }
+                                inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
+                                live = 1.0f;
                             }
-                            continue;
+                            __syncwarp();
+                            info[2 * lane] = o;
+                            info[2 * lane + 1] = make_int4(__float_as_int(inv_k), __float_as_int(live), 0, 0);
+                            __syncwarp();
                         }
+                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
 #pragma unroll
-                        for (int s8 = 0; s8 < 4; ++s8) {
-                            float4 x1[4][2], x2[4][2];
+                        for (int j0 = 0; j0 < 32; j0 += 4) {
+                            float x1[4][4], x2[4][4], ik[4], lv[4];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float4 *q1 = (const float4 *)(P1b + (size_t)sl[j] * a.d_ff + f0 + 8 * s8);
-                                const float4 *q2 = (const float4 *)(P2b + (size_t)sl[j] * a.d_ff + f0 + 8 * s8);
-                                x1[j][0] = __ldg(q1); x1[j][1] = __ldg(q1 + 1);
-                                x2[j][0] = __ldg(q2); x2[j][1] = __ldg(q2 + 1);
+                            for (int u = 0; u < 4; ++u) {
+                                const int4 o = info[2 * (j0 + u)];
+                                const int4 b = info[2 * (j0 + u) + 1];
+                                ik[u] = __int_as_float(b.x);
+                                lv[u] = __int_as_float(b.y);
+                                x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
+                                x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
+                                x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
+                                x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
                             }
-                            float p1[8] = {0, 0, 0, 0, 0, 0, 0, 0}, p2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float wj = wt[j];
-                                p1[0] = fmaf(wj, x1[j][0].x, p1[0]); p1[1] = fmaf(wj, x1[j][0].y, p1[1]);
-                                p1[2] = fmaf(wj, x1[j][0].z, p1[2]); p1[3] = fmaf(wj, x1[j][0].w, p1[3]);
-                                p1[4] = fmaf(wj, x1[j][1].x, p1[4]); p1[5] = fmaf(wj, x1[j][1].y, p1[5]);
-                                p1[6] = fmaf(wj, x1[j][1].z, p1[6]); p1[7] = fmaf(wj, x1[j][1].w, p1[7]);
-                                p2[0] = fmaf(wj, x2[j][0].x, p2[0]); p2[1] = fmaf(wj, x2[j][0].y, p2[1]);
-                                p2[2] = fmaf(wj, x2[j][0].z, p2[2]); p2[3] = fmaf(wj, x2[j][0].w, p2[3]);
-                                p2[4] = fmaf(wj, x2[j][1].x, p2[4]); p2[5] = fmaf(wj, x2[j][1].y, p2[5]);
-                                p2[6] = fmaf(wj, x2[j][1].z, p2[6]); p2[7] = fmaf(wj, x2[j][1].w, p2[7]);
+                            for (int u = 0; u < 4; ++u) {
+                                const int j = j0 + u;
+                                const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
+                                const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
+                                // reference token or exact copy: lv = 0, z = 0
+                                const float dh = (silu_fast(v1[j]) * v2[j] - silu_fast(m1) * m2) * lv[u];
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
+                                if (fok && t0 + j < a.rows) {
+                                    hi[(size_t)j * a.d_ff] = hb;
+                                    lo[(size_t)j * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                                }
                             }
-                            float h8[8], l8[8];
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float m1 = p1[j] * inv_k, m2 = p2[j] * inv_k;
-                                const float dh = silu_fast(v1[8 * s8 + j]) * v2[8 * s8 + j] - silu_fast(m1) * m2;
-                                h8[j] = __bfloat162float(__float2bfloat16_rn(dh));
-                                l8[j] = dh - h8[j];
-                            }
-                            store_bf16x8(hi + 8 * s8, h8);
-                            store_bf16x8(lo + 8 * s8, l8);
                         }
                     }
                 } else {  // M_S2
@@ -612,7 +627,9 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     __nv_bfloat16 *dh_lo = (__nv_bfloat16 *)(ws + wl.dh_lo);
     const bool fp8 = g.ref_dtype == RKV_FP8_E4M3;
     void *ref_mma = fp8 ? (void *)(ws + wl.ref_mma) : pool->ref_vec;
-    if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, s)) != cudaSuccess) return e;
+    const size_t zrow = (size_t)g.LB * g.n_ref * g.d_ff;     // the all-zero projection row
+    if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, P1 + zrow, P2 + zrow, s)) != cudaSuccess)
+        return e;
 
     UmmaArgs a{};
     a.LB = g.LB; a.B = g.B; a.T = g.T; a.W = g.W; a.d_ff = g.d_ff; a.d_c = g.d_c;
