@@ -69,8 +69,11 @@ typedef struct rkv_params {
     int32_t bits;       /* 2 or 4 [RKV §2.4]                                          */
     int32_t kv_dtype;   /* RKV_F32 or RKV_BF16: kv and compressor weights             */
     int32_t ref_dtype;  /* kv_dtype, or RKV_FP8_E4M3 (bf16 kv only) [RKV §2.4 = V-A]  */
-    int32_t stride;     /* fixed reference stride s >= 1 [RKV §2.6 = Sec. IV-A]       */
+    int32_t stride;     /* reference stride s (s0 of the dynamic schedule), >= 1      */
     int32_t first;      /* position of the first reference, 0 <= first               */
+    double  alpha;      /* stride growth; 0 = fixed stride [RKV §2.6 = Sec. IV-A]     */
+    int32_t n_sink;     /* sink tokens of the dynamic schedule, >= 0                  */
+    int32_t reserved;   /* set to 0                                                   */
 } rkv_params;
 
 /* Reference pool [RKV §2.2, §2.6 = Sec. IV-A]; filled by rkv_build_ref_pool.
@@ -98,8 +101,11 @@ typedef struct rkv_cache {
     int32_t *ref_idx;
 } rkv_cache;
 
-/* Number of references per sequence for the fixed schedule: positions first,
- * first+stride, ... < T.  Returns -1 on invalid params.                          */
+/* Reference schedule [RKV §2.6 = Sec. IV-A]: p_0 = first and
+ *   p_{m+1} = p_m + stride + floor(alpha * (p_m - n_sink)),
+ * every p_m < T; alpha = 0 is the fixed stride.  The first step must be >= 1
+ * (stride + floor(alpha (first - n_sink)) >= 1), otherwise the params are invalid.
+ * Returns the number of references per sequence, or -1 on invalid params.        */
 int32_t rkv_n_ref(const rkv_params *p);
 
 /* Host-only: bytes the caller must provide.  Any output pointer may be NULL.
@@ -109,7 +115,7 @@ int32_t rkv_n_ref(const rkv_params *p);
 rkv_status rkv_query_sizes(const rkv_params *p, size_t *pool_bytes, size_t *cache_bytes,
                            size_t *workspace_bytes);
 
-/* Step 0 of the write path: the fixed-stride schedule [RKV §2.6 = Sec. IV-A] and
+/* Step 0 of the write path: the reference schedule [RKV §2.6 = Sec. IV-A] and
  * the stored references.  kv: [L*B][T][W] in kv_dtype.  Writes every field of
  * *pool; with ref_dtype = RKV_FP8_E4M3 each reference is rounded to E4M3
  * (nearest even, saturating) and ref_sqnorm is taken over the rounded values.    */
@@ -138,7 +144,8 @@ rkv_status rkv_compress(const rkv_params *p, const void *kv, const rkv_ref_pool 
  * own record and its references, and return
  *   out_z[lb][i]    = dequantised z~ of token sel[lb][i]        ([L*B][n_sel][d_c])
  *   out_mean[lb][i] = mean of its stored references in KV space ([L*B][n_sel][W])
- * in out_dtype (RKV_F32 or RKV_BF16; fp32 arithmetic, one rounding at the end).
+ * in out_dtype (RKV_F32 or RKV_BF16): z~ by one fp32 fma per coordinate, the mean
+ * as fp32 sums in ascending slot order times 1/k, each rounded once to out_dtype.
  * sel: [L*B][n_sel] int32 token positions; an entry of -1 is padding and yields
  * zero rows; an entry >= T sets RKV_ERR_INDEX and yields zero rows.  Unselected
  * tokens' records are never read.  With n_sel = T and sel = 0..T-1 this is the

@@ -193,6 +193,8 @@ def dequantize(q, zmin, delta, group: int) -> np.ndarray:
 
 # --- per-sequence drivers -----------------------------------------------------------
 def schedule(cfg: wl.Config) -> np.ndarray:
+    if getattr(cfg, "alpha", 0.0) > 0.0:
+        return dynamic_schedule(cfg.T, cfg.stride, cfg.alpha, cfg.n_sink, cfg.first)
     return fixed_schedule(cfg.T, cfg.stride, cfg.first)
 
 

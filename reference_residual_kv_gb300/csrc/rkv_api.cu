@@ -4,10 +4,26 @@
 #include "rkv_internal.cuh"
 
 #include <limits.h>
+#include <math.h>
 
 namespace rkv {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Reference count of the schedule p_{m+1} = p_m + stride + floor(alpha (p_m - n_sink)),
+// computed with the same double arithmetic as the device schedule kernel.
+static int schedule_count(const rkv_params *p)
+{
+    if (p->T <= p->first) return 0;
+    if (p->alpha == 0.0) return (p->T - p->first + p->stride - 1) / p->stride;
+    long long pos = p->first;
+    int n = 0;
+    while (pos < p->T) {
+        ++n;
+        pos = pos + p->stride + (long long)floor(p->alpha * (double)(pos - p->n_sink));
+    }
+    return n;
+}
 
 Geometry make_geometry(const rkv_params *p)
 {
@@ -21,13 +37,15 @@ Geometry make_geometry(const rkv_params *p)
     g.d_c = p->d_c;
     g.k = p->k;
     g.bits = p->bits;
-    g.n_ref = p->T <= p->first ? 0 : (p->T - p->first + p->stride - 1) / p->stride;
+    g.n_ref = schedule_count(p);
     g.n_groups = p->d_c / 32;
     g.code_pitch = p->d_c * p->bits / 8;
     g.kv_dtype = p->kv_dtype;
     g.ref_dtype = p->ref_dtype;
     g.stride = p->stride;
     g.first = p->first;
+    g.alpha = p->alpha;
+    g.n_sink = p->n_sink;
     g.n_mtiles = (p->T + kBM - 1) / kBM;
     int max_nt = (g.n_ref + kBN - 1) / kBN;
     g.max_chunks = max_nt == 0 ? 1 : (max_nt + kDistChunk - 1) / kDistChunk;
@@ -48,6 +66,8 @@ Workspace workspace_layout(const Geometry &g)
     w.rn_max = take(LB * 4);
     w.cand = take(tc ? LB * T * g.max_chunks * kCand * 8 : 0);
     w.copy_flag = take(LB * T);
+    w.xnorm = take(tc ? LB * T * 4 : 0);
+    w.scan_list = take(tc ? (LB * T + 1) * 4 : 0);     // list, then its count
     w.dh_hi = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh_lo = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh32 = take(tc ? 0 : LB * T * g.d_ff * 4);
@@ -62,6 +82,10 @@ static rkv_status check_params(const rkv_params *p)
     if (p->L < 1 || p->B < 1 || p->T < 1 || p->N < 1 || p->D < 1 || p->d_ff < 1 || p->d_c < 1)
         return RKV_ERR_INVALID_ARG;
     if (p->stride < 1 || p->first < 0 || p->k < 1 || p->group < 1)
+        return RKV_ERR_INVALID_ARG;
+    if (!(p->alpha >= 0.0) || p->alpha > 1e6 || p->n_sink < 0) return RKV_ERR_INVALID_ARG;
+    // the schedule's steps grow with the position; the first one must advance
+    if (p->stride + (long long)floor(p->alpha * (double)(p->first - p->n_sink)) < 1)
         return RKV_ERR_INVALID_ARG;
     if (p->bits != 2 && p->bits != 4) return RKV_ERR_INVALID_ARG;
     if (p->kv_dtype != RKV_F32 && p->kv_dtype != RKV_BF16) return RKV_ERR_INVALID_ARG;

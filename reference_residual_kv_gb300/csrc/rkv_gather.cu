@@ -9,36 +9,44 @@
 // written with 16-byte stores.
 #include "rkv_internal.cuh"
 
+#include <cuda_fp16.h>
+
 namespace rkv {
 
+// Adds 8 consecutive reference values into 4 float2 accumulators with paired fp32
+// adds (one IEEE add per element, same order as scalar code).
 template <typename T> struct RefLoad;
-template <> struct RefLoad<float> {       // 8 consecutive fp32 values
-    static __device__ __forceinline__ void add(const float *p, float (&a)[8])
+template <> struct RefLoad<float> {
+    static __device__ __forceinline__ void add(const float *p, float2 (&a)[4])
     {
-        float4 u = *(const float4 *)p, v = *(const float4 *)(p + 4);
-        a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
-        a[4] += v.x; a[5] += v.y; a[6] += v.z; a[7] += v.w;
+        const float4 u = *(const float4 *)p, v = *(const float4 *)(p + 4);
+        a[0] = __fadd2_rn(a[0], make_float2(u.x, u.y));
+        a[1] = __fadd2_rn(a[1], make_float2(u.z, u.w));
+        a[2] = __fadd2_rn(a[2], make_float2(v.x, v.y));
+        a[3] = __fadd2_rn(a[3], make_float2(v.z, v.w));
     }
 };
 template <> struct RefLoad<__nv_bfloat16> {
-    static __device__ __forceinline__ void add(const __nv_bfloat16 *p, float (&a)[8])
+    static __device__ __forceinline__ void add(const __nv_bfloat16 *p, float2 (&a)[4])
     {
-        uint4 raw = *(const uint4 *)p;
-        const __nv_bfloat16 *h = (const __nv_bfloat16 *)&raw;
+        const uint4 raw = *(const uint4 *)p;
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] += __bfloat162float(h[j]);
+        for (int j = 0; j < 4; ++j)     // bf16 -> fp32 is a 16-bit shift
+            a[j] = __fadd2_rn(a[j], make_float2(__uint_as_float(w[j] << 16),
+                                                __uint_as_float(w[j] & 0xffff0000u)));
     }
 };
-template <> struct RefLoad<uint8_t> {     // FP8 E4M3
-    static __device__ __forceinline__ void add(const uint8_t *p, float (&a)[8])
+template <> struct RefLoad<uint8_t> {     // FP8 E4M3: exact in fp16, two per conversion
+    static __device__ __forceinline__ void add(const uint8_t *p, float2 (&a)[4])
     {
-        uint2 raw = *(const uint2 *)p;
-        const uint8_t *b = (const uint8_t *)&raw;
+        const uint2 raw = *(const uint2 *)p;
+        const uint32_t w[2] = {raw.x, raw.y};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            __nv_fp8_e4m3 q;
-            q.__x = b[j];
-            a[j] += (float)q;
+        for (int j = 0; j < 4; ++j) {
+            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[j >> 1] >> (16 * (j & 1))) & 0xffffu);
+            const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
+            a[j] = __fadd2_rn(a[j], __half22float2(h));
         }
     }
 };
@@ -53,14 +61,14 @@ template <> __device__ __forceinline__ void store8<float>(float *dst, const floa
 template <>
 __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&v)[8])
 {
-    __align__(16) __nv_bfloat16 o[8];
+    __align__(16) __nv_bfloat162 o[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
+    for (int j = 0; j < 4; ++j) o[j] = __float22bfloat162_rn(make_float2(v[2 * j], v[2 * j + 1]));
     *(uint4 *)dst = *(const uint4 *)o;
 }
 
 template <typename RefT, typename OutT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 5)
 k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int bits,
          int n_ref, const RefT *__restrict__ ref_vec, const uint8_t *__restrict__ codes,
          const float2 *__restrict__ hdr, const int4 *__restrict__ ref_idx, OutT *__restrict__ out_z,
@@ -113,17 +121,24 @@ k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int 
         store8(oz + c, v);
     }
 
-    // mean of the stored references, summed in ascending slot order, then / k
+    // mean of the stored references, summed in ascending slot order, times 1/k
     const RefT *rbase = ref_vec + (size_t)lb * n_ref * W;
-#pragma unroll 2
+    const float inv_k = k > 0 ? 1.0f / (float)k : 0.0f;
+    const float2 ik2 = make_float2(inv_k, inv_k);
+#pragma unroll 4
     for (int c = lane * 8; c < W; c += 256) {
-        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a);
-        const float fk = (float)k;
+            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a2);
+        float a[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = k > 0 ? __fdiv_rn(a[j], fk) : 0.0f;
+        for (int j = 0; j < 4; ++j) {
+            const float2 m = __fmul2_rn(a2[j], ik2);
+            a[2 * j] = m.x;
+            a[2 * j + 1] = m.y;
+        }
         store8(om + c, a);
     }
 }

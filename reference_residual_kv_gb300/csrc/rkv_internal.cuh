@@ -20,7 +20,8 @@ namespace rkv {
 // is accepted from the expansion only if its k-th/(k+1)-th gap exceeds twice
 // kTau * (max ||r||^2 + 2 ||x|| max ||r||); otherwise it is re-ranked with exact
 // differences.
-constexpr int kCand = 8;
+constexpr int kList = 8;                  // sorted list kept per row and column half
+constexpr int kCand = 2 * kList;          // candidate entries per row and work item
 constexpr float kTau = 1.0f / 32768.0f;   // 2^-15
 constexpr int kMaxK = 4;                  // ref_idx rows are int4
 
@@ -36,7 +37,8 @@ constexpr long long kWaitCycles = 2000000000LL;
 struct Geometry {
     int L, B, LB, T, W, d_ff, d_c, k, bits, n_ref, n_groups, code_pitch;
     int kv_dtype, ref_dtype;
-    int stride, first;
+    int stride, first, n_sink;
+    double alpha;
     int n_mtiles;        // ceil(T / 128)
     int max_chunks;      // distance work items per token tile
 };
@@ -50,6 +52,8 @@ struct Workspace {
     size_t rn_max;       // f32  [LB]
     size_t cand;         // f32x2 [LB][T][max_chunks][kCand]  (tensor-core path)
     size_t copy_flag;    // u8   [LB][T]  1: every chosen reference equals the token
+    size_t xnorm;        // f32  [LB][T]  ||x||^2 of every token (tensor-core path)
+    size_t scan_list;    // i32  [LB*T] tokens whose top-k needs a full exact scan, + count
     size_t dh_hi, dh_lo; // bf16 [LB][T][d_ff]   (tensor-core path)
     size_t dh32;         // f32  [LB][T][d_ff]   (fp32 path)
     size_t z32;          // f32  [LB][T][d_c]    (fp32 path)
@@ -82,8 +86,11 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
 // top-k finalisation shared by both paths: exact re-rank / full scan
 cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
-                                 const float2 *cand, const float *rn_max, int32_t *ref_idx,
-                                 uint8_t *copy_flag, int32_t *status, cudaStream_t s);
+                                 const float2 *cand, const float *xnorm, const float *rn_max,
+                                 int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
+                                 int32_t *scan_count, int32_t *status, cudaStream_t s);
+// ||x||^2 of every token row (bf16 kv)
+cudaError_t launch_token_norms(const Geometry &g, const void *kv, float *xnorm, cudaStream_t s);
 
 int device_sm_count();
 

@@ -78,12 +78,48 @@ __global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restri
     if (lane == 0) ref_sqnorm[(size_t)lb * n_ref + m] = acc;
 }
 
+// Dynamic stride: the positions follow a recurrence, so one thread writes them in
+// order (their number grows like log T for alpha > 0) ...
+__global__ void k_schedule_dynamic_pos(int T, int stride, int first, double alpha, int n_sink,
+                                       int n_ref, int32_t *ref_pos)
+{
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    long long p = first;
+    for (int m = 0; m < n_ref && p < T; ++m) {
+        ref_pos[m] = (int32_t)p;
+        p = p + stride + (long long)floor(alpha * (double)(p - n_sink));
+    }
+}
+
+// ... and every token finds its pool by binary search: pool_size[t] = #{m: p_m < t}.
+__global__ void k_schedule_dynamic_tok(int T, int n_ref, const int32_t *__restrict__ ref_pos,
+                                       int32_t *ref_slot, int32_t *pool_size)
+{
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    int lo = 0, hi = n_ref;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (ref_pos[mid] < t) lo = mid + 1;
+        else hi = mid;
+    }
+    pool_size[t] = lo;
+    ref_slot[t] = (lo < n_ref && ref_pos[lo] == t) ? lo : -1;
+}
+
 cudaError_t launch_build_schedule(const Geometry &g, const rkv_ref_pool *pool, cudaStream_t s)
 {
-    int n = g.T > g.n_ref ? g.T : g.n_ref;
     ProfScope prof("build_schedule", s);
-    k_schedule<<<(n + 255) / 256, 256, 0, s>>>(g.T, g.stride, g.first, g.n_ref, pool->ref_pos,
-                                               pool->ref_slot, pool->pool_size);
+    if (g.alpha == 0.0) {
+        int n = g.T > g.n_ref ? g.T : g.n_ref;
+        k_schedule<<<(n + 255) / 256, 256, 0, s>>>(g.T, g.stride, g.first, g.n_ref, pool->ref_pos,
+                                                   pool->ref_slot, pool->pool_size);
+    } else {
+        k_schedule_dynamic_pos<<<1, 32, 0, s>>>(g.T, g.stride, g.first, g.alpha, g.n_sink, g.n_ref,
+                                                pool->ref_pos);
+        k_schedule_dynamic_tok<<<(g.T + 255) / 256, 256, 0, s>>>(g.T, g.n_ref, pool->ref_pos,
+                                                                pool->ref_slot, pool->pool_size);
+    }
     return cudaGetLastError();
 }
 

@@ -8,9 +8,9 @@
 //   * if the k-th/(k+1)-th expansion gap exceeds twice the expansion error bound
 //     E = kTau (rmax + 2 sqrt(||x||^2 rmax)), rmax = max ||r||^2 of the sequence,
 //     the expansion's top-k is the exact top-k;
-//   * else, if every possible member of the exact top-k is among the candidates
-//     (all of the pool fits, or the 8th candidate is more than 2E behind the k-th),
-//     the candidates are re-ranked by exact distances;
+//   * else, if every possible member of the exact top-k is among the entries (no
+//     full list of a work item ends inside the band e <= e_k + 2E), the entries
+//     inside the band are re-ranked by exact distances;
 //   * else every reference of the pool is scanned with exact distances.
 // It also flags tokens that are bit-identical to every chosen reference: their mean
 // equals the token exactly, so z = 0 exactly [RKV §2.3], which the encoder then
@@ -18,7 +18,11 @@
 // references' projections identically, since they sit in different tile rows).
 // Exact distances sum (x - r)^2 in fp32: for bf16 data x - r is exact, each group of
 // 8 squares is added as a tree, and the warp adds its lanes as a tree.
-// Without candidates (the fp32 path) every token takes the full scan.
+// Without candidates (the fp32 path) every token takes the full scan.  On the
+// tensor-core path the (rare) full scans are deferred to k_topk_fullscan: the token
+// is appended to a list and a whole block scans its pool, eight warps in parallel
+// (near-tied clusters of FP8-rounded references otherwise leave single warps
+// scanning thousands of references one after another).
 #include "rkv_internal.cuh"
 
 namespace rkv {
@@ -117,9 +121,11 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
                 const int32_t *__restrict__ ref_slot, const int32_t *__restrict__ pool_size,
-                const float2 *__restrict__ cand, const float *__restrict__ rn_max, int LB, int T_,
+                const float2 *__restrict__ cand, const float *__restrict__ xnorm,
+                const float *__restrict__ rn_max, int LB, int T_,
                 int W, int n_ref, int k, int max_chunks, int4 *__restrict__ ref_idx,
-                uint8_t *__restrict__ copy_flag)
+                uint8_t *__restrict__ copy_flag, int32_t *__restrict__ scan_list,
+                int32_t *__restrict__ scan_count)
 {
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -147,63 +153,109 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
         for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = 0x7fffffff; }
         bool full_scan = (cand == nullptr);
         if (!full_scan) {
-            // merge the work items' candidate lists: per-lane top-kCand, then 8 warp argmins
+            // the work items' candidate entries: per chunk two sorted lists of kList
+            // (one per column half of the distance tile), up to 4 entries per lane
             const int m = t / kBM;
             const int nt = dist_ntiles(pool_size, T_, m);
             const int nch = (nt + kDistChunk - 1) / kDistChunk;
+            const int nent = nch * kCand;
             const float2 *cp = cand + ((size_t)lb * T_ + t) * max_chunks * kCand;
-            float le[kCand];
-            int ls[kCand];
-#pragma unroll
-            for (int q = 0; q < kCand; ++q) { le[q] = INFINITY; ls[q] = 0x7fffffff; }
-            for (int u = lane; u < nch * kCand; u += 32) {
-                float2 c = cp[u];
-                int s = __float_as_int(c.y);
-                if (s >= 0 && c.x < INFINITY) list_insert<kCand>(le, ls, c.x, s);
-            }
-            float ce[kCand];
-            int cs[kCand];
-            int head = 0;
-#pragma unroll
-            for (int r = 0; r < kCand; ++r) {
-                float e = INFINITY;
-                int s = 0x7fffffff;
-#pragma unroll
-                for (int q = 0; q < kCand; ++q)
-                    if (q == head) { e = le[q]; s = ls[q]; }
-                float we = e;
-                int ws = s, wl = lane;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    float oe = __shfl_xor_sync(0xffffffffu, we, o);
-                    int os = __shfl_xor_sync(0xffffffffu, ws, o);
-                    int ol = __shfl_xor_sync(0xffffffffu, wl, o);
-                    if (key_less(oe, os, we, ws)) { we = oe; ws = os; wl = ol; }
-                }
-                ce[r] = we;
-                cs[r] = ws;
-                if (wl == lane && we < INFINITY) ++head;
-            }
-            const int nvalid = pool < kCand ? pool : kCand;
-            const float xn = warp_sqnorm(x, W, lane);
-            const float rm = rn_max[lb];
-            const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
-            if (nvalid > k && ce[k] - ce[k - 1] > 2.0f * E) {
-                for (int j = 0; j < k; ++j) { be[j] = ce[j]; bs[j] = cs[j]; }
-                // possibly an exact copy of all k: confirm with exact distances
-                if (xn + ce[k - 1] <= 2.0f * E) {
-                    for (int j = 0; j < k; ++j) be[j] = warp_sqdist(x, rb + (size_t)bs[j] * W, W, lane);
-                } else {
-                    be[0] = 1.0f;   // not a copy
-                }
-            } else if (pool <= kCand || ce[kCand - 1] - ce[k - 1] > 2.0f * E) {
-                for (int r = 0; r < nvalid; ++r) {
-                    float d = warp_sqdist(x, rb + (size_t)cs[r] * W, W, lane);
-                    list_insert<kMaxK>(be, bs, d, cs[r]);
-                }
+            constexpr int EPL = 4;
+            if (nent > EPL * 32) {
+                full_scan = true;           // more entries than one warp holds
             } else {
-                full_scan = true;
+                float le[EPL];
+                int ls[EPL];
+                bool last[EPL];             // the 8th entry of a full list
+#pragma unroll
+                for (int q = 0; q < EPL; ++q) {
+                    const int u = lane + 32 * q;
+                    le[q] = INFINITY;
+                    ls[q] = 0x7fffffff;
+                    last[q] = false;
+                    if (u < nent) {
+                        const float2 c = cp[u];
+                        const int sr = __float_as_int(c.y);
+                        if (sr >= 0 && c.x < INFINITY) {
+                            le[q] = c.x;
+                            ls[q] = sr;
+                            last[q] = (u % kList) == kList - 1;
+                        }
+                    }
+                }
+                // the k + 1 smallest expansion values: rounds of warp argmin
+                float ek[kMaxK + 1];
+                int sk[kMaxK + 1];
+                bool taken[EPL] = {false, false, false, false};
+#pragma unroll
+                for (int r = 0; r <= kMaxK; ++r) {
+                    float me = INFINITY;
+                    int ms = 0x7fffffff, mq = -1;
+#pragma unroll
+                    for (int q = 0; q < EPL; ++q)
+                        if (!taken[q] && key_less(le[q], ls[q], me, ms)) { me = le[q]; ms = ls[q]; mq = q; }
+                    float we = me;
+                    int ws = ms;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float oe = __shfl_xor_sync(0xffffffffu, we, o);
+                        const int os = __shfl_xor_sync(0xffffffffu, ws, o);
+                        if (key_less(oe, os, we, ws)) { we = oe; ws = os; }
+                    }
+                    ek[r] = we;
+                    sk[r] = ws;
+#pragma unroll
+                    for (int q = 0; q < EPL; ++q)
+                        if (q == mq && ms == ws && me == we) taken[q] = true;
+                }
+                const float xn = xnorm ? xnorm[(size_t)lb * T_ + t] : warp_sqnorm(x, W, lane);
+                const float rm = rn_max[lb];
+                const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
+                float e_k = ek[0], e_k1 = ek[1];   // k-th and (k+1)-th expansion values
+#pragma unroll
+                for (int j = 1; j < kMaxK; ++j)
+                    if (j == k - 1) { e_k = ek[j]; e_k1 = ek[j + 1]; }
+                if (e_k1 - e_k > 2.0f * E) {
+#pragma unroll
+                    for (int j = 0; j < kMaxK; ++j)
+                        if (j < k) { be[j] = ek[j]; bs[j] = sk[j]; }
+                    // possibly an exact copy of all k: confirm with exact distances
+                    if (xn + e_k <= 2.0f * E) {
+#pragma unroll
+                        for (int j = 0; j < kMaxK; ++j)
+                            if (j < k) be[j] = warp_sqdist(x, rb + (size_t)bs[j] * W, W, lane);
+                    } else {
+                        be[0] = 1.0f;   // not a copy
+                    }
+                } else {
+                    // every reference that can reach the top-k has expansion <= band;
+                    // a full list whose last entry is inside the band may have dropped
+                    // some of them, otherwise they are all among the entries
+                    const float band = e_k + 2.0f * E;
+                    bool inc = false;
+#pragma unroll
+                    for (int q = 0; q < EPL; ++q) inc |= last[q] && le[q] <= band;
+                    if (__any_sync(0xffffffffu, inc)) {
+                        full_scan = true;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < EPL; ++q) {
+                            unsigned msk = __ballot_sync(0xffffffffu, le[q] <= band);
+                            while (msk) {
+                                const int src = __ffs(msk) - 1;
+                                msk &= msk - 1;
+                                const int sl = __shfl_sync(0xffffffffu, ls[q], src);
+                                const float d = warp_sqdist(x, rb + (size_t)sl * W, W, lane);
+                                list_insert<kMaxK>(be, bs, d, sl);
+                            }
+                        }
+                    }
+                }
             }
+        }
+        if (full_scan && scan_list) {
+            if (lane == 0) scan_list[atomicAdd(scan_count, 1)] = (int32_t)((size_t)lb * T_ + t);
+            return;
         }
         if (full_scan) {
             for (int s = 0; s < pool; ++s) {
@@ -212,7 +264,9 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
             }
         }
         same = 1;
-        for (int j = 0; j < k; ++j) same &= be[j] == 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+            if (j < k) same &= be[j] == 0.0f;
         // chosen slots in ascending order
         int ch[kMaxK];
 #pragma unroll
@@ -231,25 +285,168 @@ k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
     }
 }
 
+// One block per listed token: its eight warps scan slots w, w+8, ... of the pool with
+// exact distances, each keeping a top-k; warp 0 merges the eight lists.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_topk_fullscan(const T *__restrict__ kv, const T *__restrict__ refs,
+                const int32_t *__restrict__ pool_size, int T_, int W, int n_ref, int k,
+                const int32_t *__restrict__ scan_list, const int32_t *__restrict__ scan_count,
+                int4 *__restrict__ ref_idx, uint8_t *__restrict__ copy_flag)
+{
+    __shared__ float sd[8][kMaxK];
+    __shared__ int ss[8][kMaxK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = *scan_count;
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
+        const int flat = scan_list[e];
+        const int lb = flat / T_, t = flat % T_;
+        const int pool = pool_size[t];
+        const T *x = kv + (size_t)flat * W;
+        const T *rb = refs + (size_t)lb * n_ref * W;
+        float be[kMaxK];
+        int bs[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = 0x7fffffff; }
+        for (int s = warp; s < pool; s += 8) {
+            const float d = warp_sqdist(x, rb + (size_t)s * W, W, lane);
+            list_insert<kMaxK>(be, bs, d, s);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) { sd[warp][j] = be[j]; ss[warp][j] = bs[j]; }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float d = sd[lane >> 2][lane & 3];
+            int sl = ss[lane >> 2][lane & 3];
+            float cd[kMaxK];
+            int cs[kMaxK];
+#pragma unroll
+            for (int r = 0; r < kMaxK; ++r) {
+                float wd = d;
+                int ws = sl;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float od = __shfl_xor_sync(0xffffffffu, wd, o);
+                    const int os = __shfl_xor_sync(0xffffffffu, ws, o);
+                    if (key_less(od, os, wd, ws)) { wd = od; ws = os; }
+                }
+                cd[r] = wd;
+                cs[r] = ws;
+                if (sl == ws && d == wd) { d = INFINITY; sl = 0x7fffffff; }
+            }
+            int same = 1, ch[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                ch[j] = j < k ? cs[j] : 0x7fffffff;
+                if (j < k) same &= cd[j] == 0.0f;
+            }
+#pragma unroll
+            for (int a = 0; a < kMaxK; ++a)
+#pragma unroll
+                for (int b = 0; b + 1 < kMaxK - a; ++b)
+                    if (ch[b] > ch[b + 1]) { int tmp = ch[b]; ch[b] = ch[b + 1]; ch[b + 1] = tmp; }
+            if (lane == 0) {
+                ref_idx[flat] = make_int4(ch[0], k > 1 ? ch[1] : -1, k > 2 ? ch[2] : -1,
+                                          k > 3 ? ch[3] : -1);
+                copy_flag[flat] = (uint8_t)same;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ||x||^2 of every bf16 token row: one warp per row, all of a lane's 16-byte loads in
+// flight at once (the distance bound of the top-k finalisation needs it).
+template <int NV>
+__global__ void __launch_bounds__(256)
+k_token_norms(const __nv_bfloat16 *__restrict__ kv, long long rows, int W, float *__restrict__ out)
+{
+    const int lane = threadIdx.x & 31;
+    const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rows) return;
+    const __nv_bfloat16 *x = kv + (size_t)r * W;
+    float acc = 0.0f;
+    if constexpr (NV > 0) {
+        uint4 v[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) v[u] = __ldg((const uint4 *)(x + lane * 8 + u * 256));
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xffff0000u);
+                acc = fmaf(a, a, acc);
+                acc = fmaf(b, b, acc);
+            }
+        }
+    } else {
+        acc = 0.0f;
+        for (int c = lane * 8; c < W; c += 256) {
+            float a[8];
+            Vec8<__nv_bfloat16>::load(x + c, a);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = fmaf(a[j], a[j], acc);
+        }
+    }
+    acc = warp_tree_sum(acc);
+    if (lane == 0) out[r] = acc;
+}
+
+cudaError_t launch_token_norms(const Geometry &g, const void *kv, float *xnorm, cudaStream_t s)
+{
+    const long long rows = (long long)g.LB * g.T;
+    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
+    ProfScope prof("token_norms", s);
+    const __nv_bfloat16 *x = (const __nv_bfloat16 *)kv;
+    if (g.W == 2048) k_token_norms<8><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
+    else if (g.W == 1024) k_token_norms<4><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
+    else k_token_norms<0><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
-                                 const float2 *cand, const float *rn_max, int32_t *ref_idx,
-                                 uint8_t *copy_flag, int32_t *status, cudaStream_t s)
+                                 const float2 *cand, const float *xnorm, const float *rn_max,
+                                 int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
+                                 int32_t *scan_count, int32_t *status, cudaStream_t s)
 {
     (void)status;
     long long warps = (long long)g.LB * g.T;
     unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-    ProfScope prof("topk_finalize", s);
-    if (ref_exact_is_f32)
-        k_topk_finalize<float><<<blocks, 256, 0, s>>>(
-            (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size, cand,
-            rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks, (int4 *)ref_idx, copy_flag);
-    else
-        k_topk_finalize<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-            (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
-            pool->pool_size, cand, rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks,
-            (int4 *)ref_idx, copy_flag);
-    return cudaGetLastError();
+    cudaError_t e;
+    if (scan_list && (e = cudaMemsetAsync(scan_count, 0, sizeof(int32_t), s)) != cudaSuccess)
+        return e;
+    {
+        ProfScope prof("topk_finalize", s);
+        if (ref_exact_is_f32)
+            k_topk_finalize<float><<<blocks, 256, 0, s>>>(
+                (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size, cand,
+                xnorm, rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks, (int4 *)ref_idx,
+                copy_flag, scan_list, scan_count);
+        else
+            k_topk_finalize<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
+                pool->pool_size, cand, xnorm, rn_max, g.LB, g.T, g.W, g.n_ref, g.k,
+                g.max_chunks, (int4 *)ref_idx, copy_flag, scan_list, scan_count);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (scan_list) {
+        ProfScope prof("topk_fullscan", s);
+        const int grid = 2 * device_sm_count();
+        if (ref_exact_is_f32)
+            k_topk_fullscan<float><<<grid, 256, 0, s>>>(
+                (const float *)kv, (const float *)ref_exact, pool->pool_size, g.T, g.W, g.n_ref,
+                g.k, scan_list, scan_count, (int4 *)ref_idx, copy_flag);
+        else
+            k_topk_fullscan<__nv_bfloat16><<<grid, 256, 0, s>>>(
+                (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->pool_size, g.T,
+                g.W, g.n_ref, g.k, scan_list, scan_count, (int4 *)ref_idx, copy_flag);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace rkv

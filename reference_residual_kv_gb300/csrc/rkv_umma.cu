@@ -10,7 +10,8 @@
 //               while the next tile accumulates
 // The epilogue is what differs between the four uses:
 //   M_P    P1 | P2 = R [W_c1 | W_c2] for each stored reference (fp32 out)
-//   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kCand per row
+//   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kList per row
+//          and column half
 //          [RKV §2.2 = Sec. IV-A; ||x||^2 is common to a row and left out]
 //   M_S1   dh = Swish(x W_c1) ⊙ x W_c2 - Swish(p1) ⊙ p2, p = mean of the chosen
 //          references' P rows, i.e. the first layer of f_c at the KV-space mean
@@ -34,7 +35,7 @@ constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kMergeBytes = kBM * kCand * 8;
+constexpr int kMergeBytes = 8 * 1024;        // S1: per-warp token info
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kMergeBytes;
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
 // projections run transposed: D[f][t] = W[f][:] . X[t][:], two 128x128 MMAs per step
@@ -111,12 +112,6 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float (&v
     *(uint4 *)dst = *(const uint4 *)o;
 }
 
-// named barrier of the epilogue warps only
-__device__ __forceinline__ void epi_bar()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-}
-
 // Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
 __device__ __forceinline__ float silu_fast(float u)
 {
@@ -138,8 +133,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
-    volatile int *epi_abort = abort_flag + 1;
-    float2 *merge_buf = (float2 *)(tiles + kStages * kStageBytes + 256);
+    int4 *info_buf = (int4 *)(tiles + kStages * kStageBytes + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -153,7 +147,6 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         }
         um::mbar_init(drain, 1);
         *abort_flag = 0;
-        *epi_abort = 0;
         um::fence_mbar_init();
     }
     if (warp == 1) {
@@ -251,6 +244,16 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     um::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
+                    // distance tiles: only the references this CTA's token rows can see
+                    // (causal pool of its last row), N rounded up to 16; none -> no MMA
+                    uint32_t idesc = kIdesc;
+                    bool issue = true;
+                    if (MODE == M_DIST) {
+                        const int own = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1] - n * kBN;
+                        const int cols = own < kBN ? own : kBN;
+                        issue = it.m < a.n_mtiles && cols > 0;
+                        if (issue) idesc = um::idesc_bf16_f32(kBM, (cols + 15) & ~15);
+                    }
                     for (int kc = 0; kc < k_iters; ++kc) {
                         if (*abort_flag || !um::mbar_wait(&full[stage], ph, kWaitCycles)) {
                             ok = false;
@@ -268,10 +271,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                                 um::mma_bf16(d_tmem, w1 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
                                 um::mma_bf16(d_tmem + kBN / 2, w2 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
                             }
-                        } else {
+                        } else if (issue) {
 #pragma unroll
                             for (int k = 0; k < kBK / 16; ++k)
-                                um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                                um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
                         }
                         if (C > 1) um::mma_commit_mc(&empty[stage], kMask);
                         else um::mma_commit(&empty[stage]);
@@ -306,12 +309,12 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const int r = it.m * kBM + row;
             const bool in = r < a.rows;
 
-            float be[kCand];
-            int bs[kCand];
+            float be[kList];
+            int bs[kList];
             int pool = 0, tile_pool = 0;
             if (MODE == M_DIST) {
 #pragma unroll
-                for (int j = 0; j < kCand; ++j) { be[j] = INFINITY; bs[j] = -1; }
+                for (int j = 0; j < kList; ++j) { be[j] = INFINITY; bs[j] = -1; }
                 pool = in ? a.pool_size[r] : 0;
                 tile_pool = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1];
             }
@@ -360,13 +363,13 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         for (int j = 0; j < 32; ++j) {
                             const float rj = __shfl_sync(0xffffffffu, rn_l, j);
                             const float e = fmaf(-2.0f, v[j], rj);
-                            if (s0 + j < pool && e < be[kCand - 1]) {
+                            if (s0 + j < pool && e < be[kList - 1]) {
                                 // this warp's slots arrive in increasing order: strict <
                                 // keeps the lower slot ahead of an equal later one
                                 float ce = e;
                                 int cs = s0 + j;
 #pragma unroll
-                                for (int qq = 0; qq < kCand; ++qq) {
+                                for (int qq = 0; qq < kList; ++qq) {
                                     const bool lt = ce < be[qq];
                                     const float te = lt ? be[qq] : ce;
                                     const int ts = lt ? bs[qq] : cs;
@@ -386,7 +389,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const bool fok = f < a.d_ff;
                     const float *P1f = a.P1 + (fok ? f : 0);
                     const float *P2f = a.P2 + (fok ? f : 0);
-                    int4 *info = (int4 *)merge_buf + (warp - 2) * 64;   // 32 tokens x 2 int4
+                    int4 *info = info_buf + (warp - 2) * 64;   // 32 tokens x 2 int4
                     const int zoff = a.LB * a.n_ref * a.d_ff;
                     const int lboff = it.lb * a.n_ref;
 #pragma unroll 1
@@ -479,47 +482,17 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 um::mbar_arrive(&tempty[buf]);
                 ++cnt;
             }
-            if (MODE == M_DIST) {
-                // merge the two column halves' lists of each row.  Every epilogue warp
-                // passes the three barriers once per item, also when aborting; the
-                // decision to stop comes from a flag that only epilogue warps write,
-                // and only before the first barrier, so all of them read one value.
-                if (!ok) *epi_abort = 1;
-                epi_bar();
-                const bool stop = *epi_abort != 0;
-                if (!stop && h == 1) {
+            if (MODE == M_DIST && ok && in) {
+                // this warp's sorted list (its half of the columns) as is; the two
+                // halves' lists stay separate: [chunk][h * kList + j]
+                float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand +
+                                        h * kList);
 #pragma unroll
-                    for (int j = 0; j < kCand; ++j) merge_buf[row * kCand + j] = make_float2(be[j], __int_as_float(bs[j]));
-                }
-                epi_bar();
-                if (!stop && h == 0 && in) {
-#pragma unroll
-                    for (int j = 0; j < kCand; ++j) {
-                        const float2 o = merge_buf[row * kCand + j];
-                        float ce = o.x;
-                        int cs = __float_as_int(o.y);
-                        if (cs < 0) break;
-#pragma unroll
-                        for (int qq = 0; qq < kCand; ++qq) {
-                            const bool lt = ce < be[qq] || (ce == be[qq] && (unsigned)cs < (unsigned)bs[qq]);
-                            const float te = lt ? be[qq] : ce;
-                            const int ts = lt ? bs[qq] : cs;
-                            if (lt) { be[qq] = ce; bs[qq] = cs; }
-                            ce = te;
-                            cs = ts;
-                        }
-                    }
-                    float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand);
-#pragma unroll
-                    for (int j = 0; j < kCand / 2; ++j)
-                        cp[j] = make_float4(be[2 * j], __int_as_float(bs[2 * j]), be[2 * j + 1],
-                                            __int_as_float(bs[2 * j + 1]));
-                }
-                epi_bar();
-                if (stop) { ok = false; break; }
-            } else if (!ok) {
-                break;
+                for (int j = 0; j < kList / 2; ++j)
+                    cp[j] = make_float4(be[2 * j], __int_as_float(bs[2 * j]), be[2 * j + 1],
+                                        __int_as_float(bs[2 * j + 1]));
             }
+            if (!ok) break;
         }
         if (!ok) {
             set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
@@ -669,8 +642,12 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         d.k_chunks = kw; d.a_sources = 1; d.b_split = 0; d.b_per_layer = 0;
         if ((e = run<M_DIST>(mX, mX, mRb, mRb, d, s)) != cudaSuccess) return e;
     }
-    if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, rn_max, cache->ref_idx,
-                                  copy_flag, status, s)) != cudaSuccess)
+    int32_t *scan_list = (int32_t *)(ws + wl.scan_list);
+    float *xnorm = (float *)(ws + wl.xnorm);
+    if (g.n_ref > 0 && (e = launch_token_norms(g, kv, xnorm, s)) != cudaSuccess) return e;
+    if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, xnorm, rn_max, cache->ref_idx,
+                                  copy_flag, scan_list, scan_list + (size_t)g.LB * g.T, status,
+                                  s)) != cudaSuccess)
         return e;
     {
         UmmaArgs p = a;

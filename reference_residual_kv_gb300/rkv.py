@@ -25,7 +25,8 @@ _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 class rkv_params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "L", "B", "T", "N", "D", "d_ff", "d_c", "k", "group", "bits", "kv_dtype", "ref_dtype",
-        "stride", "first")]
+        "stride", "first")] + [("alpha", ctypes.c_double), ("n_sink", ctypes.c_int32),
+                               ("reserved", ctypes.c_int32)]
 
 
 class rkv_ref_pool(ctypes.Structure):
@@ -100,16 +101,18 @@ def _stream(stream) -> int | None:
 
 
 def make_params(L, B, T, N, D, d_ff, d_c, k=4, group=32, bits=4, kv_dtype="bf16",
-                ref_dtype=None, stride=8, first=0) -> rkv_params:
+                ref_dtype=None, stride=8, first=0, alpha=0.0, n_sink=0) -> rkv_params:
     kd = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else kv_dtype
     rd = kd if ref_dtype is None else (_DTYPES[ref_dtype] if isinstance(ref_dtype, str) else ref_dtype)
-    return rkv_params(L, B, T, N, D, d_ff, d_c, k, group, bits, kd, rd, stride, first)
+    return rkv_params(L, B, T, N, D, d_ff, d_c, k, group, bits, kd, rd, stride, first, float(alpha),
+                      n_sink, 0)
 
 
 def params_from_config(cfg) -> rkv_params:
     """rkv_params from a workload description with the same field names."""
     return make_params(cfg.L, cfg.B, cfg.T, cfg.N, cfg.D, cfg.d_ff, cfg.d_c, cfg.k, cfg.group,
-                       cfg.bits, cfg.kv_dtype, cfg.ref_dtype, cfg.stride, cfg.first)
+                       cfg.bits, cfg.kv_dtype, cfg.ref_dtype, cfg.stride, cfg.first,
+                       getattr(cfg, "alpha", 0.0), getattr(cfg, "n_sink", 0))
 
 
 # ---- entry points (same names as the C ABI) -------------------------------------------

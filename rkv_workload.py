@@ -120,8 +120,10 @@ class Config:
     k: int = 4
     group: int = 32
     bits: int = 4
-    stride: int = 8
+    stride: int = 8             # fixed stride, or s0 of the dynamic schedule
     first: int = 0
+    alpha: float = 0.0          # dynamic-stride growth (0: fixed stride)
+    n_sink: int = 0
     kv_dtype: str = "bf16"      # 'f32' or 'bf16' (kv and compressor weights)
     ref_dtype: str = "bf16"     # same as kv_dtype, or 'fp8' (OCP E4M3)
     recipe: str = "text"        # 'centroids' | 'text' | 'multimodal'
@@ -141,10 +143,6 @@ class Config:
     @property
     def W(self) -> int:
         return 2 * self.N * self.D
-
-    @property
-    def n_ref(self) -> int:
-        return 0 if self.T <= self.first else (self.T - self.first + self.stride - 1) // self.stride
 
     def replace(self, **kw) -> "Config":
         return dataclasses.replace(self, **kw)
@@ -185,12 +183,34 @@ def image_segments(cfg: Config):
             for m in range(cfg.n_seg)]
 
 
+def _normal_rows(key: int, T: int, W: int, threads: int = 0) -> np.ndarray:
+    """normal(key, T*W) as [T][W], drawn in row blocks on several threads (the stream is
+    counter-based, so the values do not depend on the blocking)."""
+    if threads <= 1 or T * W < (1 << 24):
+        return normal(key, T * W).reshape(T, W)
+    import concurrent.futures as cf
+    out = np.empty((T, W), dtype=np.float64)
+    step = max(1, T // (4 * threads))
+
+    def fill(r0):
+        r1 = min(T, r0 + step)
+        out[r0:r1] = normal(key, (r1 - r0) * W, r0 * W).reshape(r1 - r0, W)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(fill, range(0, T, step)))
+    return out
+
+
+GEN_THREADS = 16
+
+
 def sequence_kv64(cfg: Config, layer: int, seq: int) -> np.ndarray:
     """Unrounded float64 kv rows [T][W] of one (layer, sequence)."""
     T, W = cfg.T, cfg.W
     s = cfg.seed
     kv = np.empty((T, W), dtype=np.float64)
-    noise = normal(stream_key(s, TAG_NOISE, layer, seq), T * W).reshape(T, W)
+    threads = GEN_THREADS if cfg.L * cfg.B == 1 else 0
+    noise = _normal_rows(stream_key(s, TAG_NOISE, layer, seq), T, W, threads)
     if cfg.recipe == "centroids":
         cent = normal(stream_key(s, TAG_CENT, layer, seq), cfg.n_cent * W).reshape(cfg.n_cent, W)
         cid = np.minimum((uniform(stream_key(s, TAG_CID, layer, seq), T) * cfg.n_cent).astype(np.int64),

@@ -86,3 +86,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rkv, "_lib", None)
     with pytest.raises(RuntimeError):
         rkv.lib()
+
+
+def test_dynamic_schedule_counts_host_side(lib):
+    # rkv_n_ref follows the dynamic recurrence [RKV §2.6]; under the Table VI reading
+    # (s0 = 10, n_sink = 0, 261888 scheduled positions) it gives the table's counts
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "table6_ref_counts.json")))
+    for alpha, n in zip(g["alpha"], g["n_ref"]):
+        p = rkv.make_params(1, 1, g["T"], 1, 4, 32, 32, stride=g["s0"], alpha=alpha, n_sink=g["n_sink"])
+        assert rkv.rkv_n_ref(p) == n
+
+
+def test_dynamic_schedule_rejects_non_advancing_first_step(lib):
+    # stride + floor(alpha (first - n_sink)) < 1 would not advance
+    p = rkv.make_params(1, 1, 1000, 1, 4, 32, 32, stride=1, alpha=1.0, n_sink=10)
+    assert rkv.rkv_n_ref(p) == -1
+    a = ctypes.c_size_t()
+    assert lib.rkv_query_sizes(ctypes.byref(p), ctypes.byref(a), None, None) == rkv.RKV_ERR_INVALID_ARG

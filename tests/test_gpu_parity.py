@@ -88,6 +88,35 @@ def test_edge_cases_small_T_first_offset_k():
             assert np.all(gpu["idx"][0][: cfg.first] == -1)
 
 
+def test_dynamic_schedule_matches_oracle_and_table6():
+    # the device schedule (recurrence on one thread, pools by binary search) equals the
+    # oracle's, and reproduces Table VI's reference counts under the stated reading
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "table6_ref_counts.json")))
+    for alpha, n in zip(g["alpha"][1:], g["n_ref"][1:]):
+        cfg = wl.CONFIGS["tiny-fp32"].replace(T=g["T"], N=1, D=4, d_ff=32, d_c=32, stride=g["s0"],
+                                             alpha=alpha, n_sink=g["n_sink"])
+        p = rkv.params_from_config(cfg)
+        bufs = rkv.Buffers(p)
+        kv = torch.zeros((1, cfg.T, cfg.W), dtype=torch.float32, device="cuda")
+        bufs.build_ref_pool(kv)
+        torch.cuda.synchronize()
+        ref_pos = oracle.schedule(cfg)
+        assert bufs.n_ref == n == ref_pos.size
+        assert np.array_equal(bufs.ref_pos.cpu().numpy()[:n], ref_pos)
+        ps = bufs.pool_size.cpu().numpy()
+        assert np.array_equal(ps, np.searchsorted(ref_pos, np.arange(cfg.T), side="left"))
+        slot = bufs.ref_slot.cpu().numpy()
+        assert np.array_equal(np.nonzero(slot >= 0)[0], ref_pos) and np.array_equal(slot[ref_pos], np.arange(n))
+
+
+def test_dynamic_schedule_write_path_parity():
+    cfg = C["llama3.1-8b-kv"].replace(L=1, T=3000, stride=10, alpha=0.05, n_sink=4)
+    _parity(cfg, n_sample=120, all_idx=True)
+    cfg = C["long-131k-fp8ref"].replace(T=5000, stride=12, alpha=0.02)
+    _parity(cfg, n_sample=80, all_idx=True)
+
+
 def test_constant_group_and_ties():
     # token 3 is a copy of reference 0 (its only pool member): z = 0 exactly and
     # every group is constant; references 5, 6, 7 duplicate reference 4, so the
@@ -105,6 +134,23 @@ def test_constant_group_and_ties():
     assert gpu["idx"][0, 300].tolist() == [4, 5, 6, 7]
     check_all_indices(cfg, kv[0][0], gpu["idx"][0])
     check_tokens(cfg, kv[0][0], w[0], gpu, 0, np.array([3, 300, 301]))
+
+
+def test_many_tied_references_take_the_block_scan():
+    # references 4..15 are identical and token 300 sits on them: all eight expansion
+    # candidates tie, so the top-k is settled by the exact block scan (lowest slots win)
+    cfg = C["llama3.1-8b-kv"].replace(L=1, T=640, N=2, D=64, d_ff=256, d_c=64)
+    kv, w = gen_inputs(cfg)
+    kv[0] = kv[0].copy()
+    for s in range(5, 16):
+        kv[0][0, 8 * s] = kv[0][0, 32]
+    kv[0][0, 300] = kv[0][0, 32]
+    kv[0][0, 301] = kv[0][0, 32] ^ np.uint16(1)        # one bit away from the cluster
+    bufs, _ = run_gpu(cfg, kv, w)
+    gpu = host_records(cfg, bufs)
+    assert gpu["idx"][0, 300].tolist() == [4, 5, 6, 7]
+    check_all_indices(cfg, kv[0][0], gpu["idx"][0])
+    check_tokens(cfg, kv[0][0], w[0], gpu, 0, np.array([300, 301, 302, 639]))
 
 
 def test_records_requantise_bit_exactly_from_gpu_z():
