@@ -145,10 +145,24 @@ __device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, ui
     }
     const float dl = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
     delta = dl;
+    // u = RN(RN((v - lo)/delta) + 1/2) < 16 is first estimated with RN(1/delta) and a
+    // multiplication: the estimate lies within 2^-18 of u (two relative roundings of
+    // 2^-24 on a quotient <= 15, plus half-ulp roundings <= 2^-21 each), so floor can
+    // differ only where the estimate is within 2^-17 of an integer; there (and where
+    // delta is too small for a finite reciprocal) the correctly rounded division is
+    // used.
+    const float rdl = __frcp_rn(dl);
+    const bool fast = dl >= 0x1p-100f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        float u = __fadd_rn(__fdiv_rn(__fsub_rn(v[j], lo), dl), 0.5f);
-        int q = (int)floorf(u);
+        const float d = __fsub_rn(v[j], lo);
+        float u = __fadd_rn(__fmul_rn(d, rdl), 0.5f);
+        float fu = floorf(u);
+        if (!fast || __fsub_rn(u, fu) < 0x1p-17f || __fsub_rn(u, fu) > 1.0f - 0x1p-17f) {
+            u = __fadd_rn(__fdiv_rn(d, dl), 0.5f);
+            fu = floorf(u);
+        }
+        int q = (int)fu;
         q = q < 0 ? 0 : (q > qmax ? qmax : q);
         if (bits == 4)
             w[j >> 3] |= (uint32_t)q << (4 * (j & 7));

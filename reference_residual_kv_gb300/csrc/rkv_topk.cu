@@ -3,14 +3,14 @@
 //   squared L2, ties to the lower slot, stored in ascending slot order.
 //
 // The tensor-core pass ranks references by the expansion ||r||^2 - 2 x.r (the
-// ||x||^2 term is common to a row) and keeps each work item's best kCand.  Here one
-// warp per token merges those candidates and decides:
+// ||x||^2 term is common to a row); every work item leaves two sorted lists of its
+// kList best per token.  Here one thread per token merges those lists and decides:
 //   * if the k-th/(k+1)-th expansion gap exceeds twice the expansion error bound
 //     E = kTau (rmax + 2 sqrt(||x||^2 rmax)), rmax = max ||r||^2 of the sequence,
 //     the expansion's top-k is the exact top-k;
 //   * else, if every possible member of the exact top-k is among the entries (no
-//     full list of a work item ends inside the band e <= e_k + 2E), the entries
-//     inside the band are re-ranked by exact distances;
+//     full list ends inside the band e <= e_k + 2E), the entries inside the band are
+//     re-ranked by exact distances (the warp serves such tokens one after another);
 //   * else every reference of the pool is scanned with exact distances.
 // It also flags tokens that are bit-identical to every chosen reference: their mean
 // equals the token exactly, so z = 0 exactly [RKV §2.3], which the encoder then
@@ -18,11 +18,11 @@
 // references' projections identically, since they sit in different tile rows).
 // Exact distances sum (x - r)^2 in fp32: for bf16 data x - r is exact, each group of
 // 8 squares is added as a tree, and the warp adds its lanes as a tree.
-// Without candidates (the fp32 path) every token takes the full scan.  On the
-// tensor-core path the (rare) full scans are deferred to k_topk_fullscan: the token
-// is appended to a list and a whole block scans its pool, eight warps in parallel
-// (near-tied clusters of FP8-rounded references otherwise leave single warps
-// scanning thousands of references one after another).
+// Without candidates (the fp32 path) every token takes the full scan, one warp per
+// token.  On the tensor-core path the (rare) full scans are deferred to
+// k_topk_fullscan: the token is appended to a list and a whole block scans its pool,
+// eight warps in parallel (near-tied clusters of FP8-rounded references otherwise
+// leave single warps scanning thousands of references one after another).
 #include "rkv_internal.cuh"
 
 namespace rkv {
@@ -117,171 +117,190 @@ __device__ __forceinline__ void list_insert(float (&le)[N], int (&ls)[N], float 
     }
 }
 
+constexpr int kNoSlot = 0x7fffffff;
+
+// Writes a token's choice: the chosen slots in ascending order, -1 for unused places.
+__device__ __forceinline__ void store_choice(int4 *ref_idx, uint8_t *copy_flag, long long g,
+                                             const int (&c)[kMaxK], int same)
+{
+    int a[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) a[j] = c[j];
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i)
+#pragma unroll
+        for (int j = 0; j + 1 < kMaxK - i; ++j)
+            if (a[j] > a[j + 1]) { const int tmp = a[j]; a[j] = a[j + 1]; a[j + 1] = tmp; }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) a[j] = a[j] == kNoSlot ? -1 : a[j];
+    ref_idx[g] = make_int4(a[0], a[1], a[2], a[3]);
+    copy_flag[g] = (uint8_t)same;
+}
+
+// fp32 path: one warp per token scans its whole pool with exact distances.
 template <typename T>
 __global__ void __launch_bounds__(256)
-k_topk_finalize(const T *__restrict__ kv, const T *__restrict__ refs,
-                const int32_t *__restrict__ ref_slot, const int32_t *__restrict__ pool_size,
-                const float2 *__restrict__ cand, const float *__restrict__ xnorm,
-                const float *__restrict__ rn_max, int LB, int T_,
-                int W, int n_ref, int k, int max_chunks, int4 *__restrict__ ref_idx,
-                uint8_t *__restrict__ copy_flag, int32_t *__restrict__ scan_list,
-                int32_t *__restrict__ scan_count)
+k_topk_scan_warp(const T *__restrict__ kv, const T *__restrict__ refs,
+                 const int32_t *__restrict__ ref_slot, const int32_t *__restrict__ pool_size,
+                 int LB, int T_, int W, int n_ref, int k, int4 *__restrict__ ref_idx,
+                 uint8_t *__restrict__ copy_flag)
 {
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (gw >= (long long)LB * T_) return;
     const int lb = (int)(gw / T_), t = (int)(gw % T_);
-
-    int out[4] = {-1, -1, -1, -1};
-    int same = 0;
     const int own = ref_slot[t];
     const int pool = pool_size[t];
-    const T *x = kv + ((size_t)lb * T_ + t) * W;
+    const T *x = kv + (size_t)gw * W;
     const T *rb = refs + (size_t)lb * n_ref * W;
+    float be[kMaxK];
+    int bs[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = kNoSlot; }
+    int same = 0;
     if (own >= 0) {
-        out[0] = own;
-    } else if (pool <= k) {
-        same = pool > 0;
-        for (int j = 0; j < pool; ++j) {
-            out[j] = j;
-            same &= warp_sqdist(x, rb + (size_t)j * W, W, lane) == 0.0f;
-        }
+        bs[0] = own;
     } else {
-        float be[kMaxK];
-        int bs[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = 0x7fffffff; }
-        bool full_scan = (cand == nullptr);
-        if (!full_scan) {
-            // the work items' candidate entries: per chunk two sorted lists of kList
-            // (one per column half of the distance tile), up to 4 entries per lane
-            const int m = t / kBM;
-            const int nt = dist_ntiles(pool_size, T_, m);
-            const int nch = (nt + kDistChunk - 1) / kDistChunk;
-            const int nent = nch * kCand;
-            const float2 *cp = cand + ((size_t)lb * T_ + t) * max_chunks * kCand;
-            constexpr int EPL = 4;
-            if (nent > EPL * 32) {
-                full_scan = true;           // more entries than one warp holds
-            } else {
-                float le[EPL];
-                int ls[EPL];
-                bool last[EPL];             // the 8th entry of a full list
-#pragma unroll
-                for (int q = 0; q < EPL; ++q) {
-                    const int u = lane + 32 * q;
-                    le[q] = INFINITY;
-                    ls[q] = 0x7fffffff;
-                    last[q] = false;
-                    if (u < nent) {
-                        const float2 c = cp[u];
-                        const int sr = __float_as_int(c.y);
-                        if (sr >= 0 && c.x < INFINITY) {
-                            le[q] = c.x;
-                            ls[q] = sr;
-                            last[q] = (u % kList) == kList - 1;
-                        }
-                    }
-                }
-                // the k + 1 smallest expansion values: rounds of warp argmin
-                float ek[kMaxK + 1];
-                int sk[kMaxK + 1];
-                bool taken[EPL] = {false, false, false, false};
-#pragma unroll
-                for (int r = 0; r <= kMaxK; ++r) {
-                    float me = INFINITY;
-                    int ms = 0x7fffffff, mq = -1;
-#pragma unroll
-                    for (int q = 0; q < EPL; ++q)
-                        if (!taken[q] && key_less(le[q], ls[q], me, ms)) { me = le[q]; ms = ls[q]; mq = q; }
-                    float we = me;
-                    int ws = ms;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float oe = __shfl_xor_sync(0xffffffffu, we, o);
-                        const int os = __shfl_xor_sync(0xffffffffu, ws, o);
-                        if (key_less(oe, os, we, ws)) { we = oe; ws = os; }
-                    }
-                    ek[r] = we;
-                    sk[r] = ws;
-#pragma unroll
-                    for (int q = 0; q < EPL; ++q)
-                        if (q == mq && ms == ws && me == we) taken[q] = true;
-                }
-                const float xn = xnorm ? xnorm[(size_t)lb * T_ + t] : warp_sqnorm(x, W, lane);
-                const float rm = rn_max[lb];
-                const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
-                float e_k = ek[0], e_k1 = ek[1];   // k-th and (k+1)-th expansion values
-#pragma unroll
-                for (int j = 1; j < kMaxK; ++j)
-                    if (j == k - 1) { e_k = ek[j]; e_k1 = ek[j + 1]; }
-                if (e_k1 - e_k > 2.0f * E) {
-#pragma unroll
-                    for (int j = 0; j < kMaxK; ++j)
-                        if (j < k) { be[j] = ek[j]; bs[j] = sk[j]; }
-                    // possibly an exact copy of all k: confirm with exact distances
-                    if (xn + e_k <= 2.0f * E) {
-#pragma unroll
-                        for (int j = 0; j < kMaxK; ++j)
-                            if (j < k) be[j] = warp_sqdist(x, rb + (size_t)bs[j] * W, W, lane);
-                    } else {
-                        be[0] = 1.0f;   // not a copy
-                    }
-                } else {
-                    // every reference that can reach the top-k has expansion <= band;
-                    // a full list whose last entry is inside the band may have dropped
-                    // some of them, otherwise they are all among the entries
-                    const float band = e_k + 2.0f * E;
-                    bool inc = false;
-#pragma unroll
-                    for (int q = 0; q < EPL; ++q) inc |= last[q] && le[q] <= band;
-                    if (__any_sync(0xffffffffu, inc)) {
-                        full_scan = true;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < EPL; ++q) {
-                            unsigned msk = __ballot_sync(0xffffffffu, le[q] <= band);
-                            while (msk) {
-                                const int src = __ffs(msk) - 1;
-                                msk &= msk - 1;
-                                const int sl = __shfl_sync(0xffffffffu, ls[q], src);
-                                const float d = warp_sqdist(x, rb + (size_t)sl * W, W, lane);
-                                list_insert<kMaxK>(be, bs, d, sl);
-                            }
-                        }
-                    }
-                }
-            }
+        for (int s = 0; s < pool; ++s) {
+            const float d = warp_sqdist(x, rb + (size_t)s * W, W, lane);
+            list_insert<kMaxK>(be, bs, d, s);
         }
-        if (full_scan && scan_list) {
-            if (lane == 0) scan_list[atomicAdd(scan_count, 1)] = (int32_t)((size_t)lb * T_ + t);
-            return;
+        same = pool > 0;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) same &= (j >= pool) || be[j] == 0.0f;
+            else bs[j] = kNoSlot;
         }
-        if (full_scan) {
-            for (int s = 0; s < pool; ++s) {
-                float d = warp_sqdist(x, rb + (size_t)s * W, W, lane);
-                list_insert<kMaxK>(be, bs, d, s);
-            }
-        }
-        same = 1;
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-            if (j < k) same &= be[j] == 0.0f;
-        // chosen slots in ascending order
-        int ch[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) ch[j] = j < k ? bs[j] : 0x7fffffff;
-#pragma unroll
-        for (int a = 0; a < kMaxK; ++a)
-#pragma unroll
-            for (int b = 0; b + 1 < kMaxK - a; ++b)
-                if (ch[b] > ch[b + 1]) { int tmp = ch[b]; ch[b] = ch[b + 1]; ch[b + 1] = tmp; }
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) out[j] = j < k ? ch[j] : -1;
     }
-    if (lane == 0) {
-        ref_idx[(size_t)lb * T_ + t] = make_int4(out[0], out[1], out[2], out[3]);
-        copy_flag[(size_t)lb * T_ + t] = (uint8_t)same;
+    if (lane == 0) store_choice(ref_idx, copy_flag, gw, bs, same);
+}
+
+// Tensor-core path.  One thread per token makes the decision from its work items'
+// sorted lists (a merge of list heads with early exit, so it reads only the entries that
+// can enter the top k + 1); the few tokens that need exact distances (a re-rank inside
+// the band, or the confirmation of an exact copy) are then served one after another by
+// the whole warp; tokens whose candidates may be incomplete go to the full-scan list.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
+              const int32_t *__restrict__ ref_slot, const int32_t *__restrict__ pool_size,
+              const float2 *__restrict__ cand, const float *__restrict__ xnorm,
+              const float *__restrict__ rn_max, int LB, int T_, int W, int n_ref, int k,
+              int max_chunks, int4 *__restrict__ ref_idx, uint8_t *__restrict__ copy_flag,
+              int32_t *__restrict__ scan_list, int32_t *__restrict__ scan_count)
+{
+    enum { kNone = 0, kDone, kRerank, kCopyCheck, kFull };
+    const int lane = threadIdx.x & 31;
+    const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    int state = kNone, lb = 0, nlists = 0;
+    int ch[kMaxK] = {kNoSlot, kNoSlot, kNoSlot, kNoSlot};
+    float band = 0.0f;
+    if (gt < (long long)LB * T_) {
+        lb = (int)(gt / T_);
+        const int t = (int)(gt % T_);
+        const int own = ref_slot[t];
+        const int pool = pool_size[t];
+        if (own >= 0) {
+            ch[0] = own;
+            state = kDone;
+        } else if (pool <= k) {
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) ch[j] = j < pool ? j : kNoSlot;
+            state = pool > 0 ? kCopyCheck : kDone;
+        } else {
+            const int nch = (dist_ntiles(pool_size, T_, t / kBM) + kDistChunk - 1) / kDistChunk;
+            nlists = 2 * nch;
+            const float4 *cp = (const float4 *)(cand + (size_t)gt * max_chunks * kCand);
+            float te[kMaxK + 1];
+            int ts[kMaxK + 1];
+#pragma unroll
+            for (int j = 0; j <= kMaxK; ++j) { te[j] = INFINITY; ts[j] = kNoSlot; }
+            float e_last = INFINITY;   // smallest last entry of a full list
+            for (int li = 0; li < nlists; ++li) {
+                const float4 *lp = cp + li * (kList / 2);
+                const float4 tail = lp[kList / 2 - 1];
+                if (__float_as_int(tail.w) >= 0) e_last = fminf(e_last, tail.z);
+                for (int j = 0; j < kList / 2; ++j) {
+                    const float4 c = j == kList / 2 - 1 ? tail : lp[j];
+                    const int s0 = __float_as_int(c.y), s1 = __float_as_int(c.w);
+                    if (s0 < 0 || !key_less(c.x, s0, te[kMaxK], ts[kMaxK])) break;
+                    list_insert<kMaxK + 1>(te, ts, c.x, s0);
+                    if (s1 < 0 || !key_less(c.z, s1, te[kMaxK], ts[kMaxK])) break;
+                    list_insert<kMaxK + 1>(te, ts, c.z, s1);
+                }
+            }
+            const float xn = xnorm[gt];
+            const float rm = rn_max[lb];
+            const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
+            float e_k = te[0], e_k1 = te[1];   // k-th and (k+1)-th expansion values
+#pragma unroll
+            for (int j = 1; j < kMaxK; ++j)
+                if (j == k - 1) { e_k = te[j]; e_k1 = te[j + 1]; }
+            if (e_k1 - e_k > 2.0f * E) {
+                // the expansion's top-k is the exact top-k; an exact copy of all k is
+                // possible only if the distance estimate is within the error bound
+#pragma unroll
+                for (int j = 0; j < kMaxK; ++j) ch[j] = j < k ? ts[j] : kNoSlot;
+                state = xn + e_k <= 2.0f * E ? kCopyCheck : kDone;
+            } else {
+                // every reference that can reach the exact top-k has expansion <= band;
+                // a full list whose last entry is inside the band may have dropped some
+                band = e_k + 2.0f * E;
+                state = e_last <= band ? kFull : kRerank;
+            }
+        }
+        if (state == kDone) store_choice(ref_idx, copy_flag, gt, ch, 0);
+        if (state == kFull) scan_list[atomicAdd(scan_count, 1)] = (int32_t)gt;
+    }
+
+    unsigned need = __ballot_sync(0xffffffffu, state == kRerank || state == kCopyCheck);
+    while (need) {
+        const int src = __ffs(need) - 1;
+        need &= need - 1;
+        const int st = __shfl_sync(0xffffffffu, state, src);
+        const long long g = __shfl_sync(0xffffffffu, gt, src);
+        const int glb = __shfl_sync(0xffffffffu, lb, src);
+        const T *x = kv + (size_t)g * W;
+        const T *rb = refs + (size_t)glb * n_ref * W;
+        int cs[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) cs[j] = __shfl_sync(0xffffffffu, ch[j], src);
+        int same = 1;
+        if (st == kCopyCheck) {
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+                if (cs[j] != kNoSlot) same &= warp_sqdist(x, rb + (size_t)cs[j] * W, W, lane) == 0.0f;
+        } else {
+            const float bd = __shfl_sync(0xffffffffu, band, src);
+            const int nent = __shfl_sync(0xffffffffu, nlists, src) * kList;
+            const float2 *cp = cand + (size_t)g * max_chunks * kCand;
+            float be[kMaxK];
+            int bs[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = kNoSlot; }
+            for (int b = 0; b < nent; b += 32) {
+                float e = INFINITY;
+                int sl = -1;
+                if (b + lane < nent) {
+                    const float2 c = cp[b + lane];
+                    e = c.x;
+                    sl = __float_as_int(c.y);
+                }
+                unsigned in = __ballot_sync(0xffffffffu, sl >= 0 && e <= bd);
+                while (in) {
+                    const int q = __ffs(in) - 1;
+                    in &= in - 1;
+                    const int s = __shfl_sync(0xffffffffu, sl, q);
+                    list_insert<kMaxK>(be, bs, warp_sqdist(x, rb + (size_t)s * W, W, lane), s);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                cs[j] = j < k ? bs[j] : kNoSlot;
+                if (j < k) same &= be[j] == 0.0f;
+            }
+        }
+        if (lane == 0) store_choice(ref_idx, copy_flag, g, cs, same);
     }
 }
 
@@ -421,16 +440,21 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
         return e;
     {
         ProfScope prof("topk_finalize", s);
-        if (ref_exact_is_f32)
-            k_topk_finalize<float><<<blocks, 256, 0, s>>>(
-                (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size, cand,
-                xnorm, rn_max, g.LB, g.T, g.W, g.n_ref, g.k, g.max_chunks, (int4 *)ref_idx,
-                copy_flag, scan_list, scan_count);
-        else
-            k_topk_finalize<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        if (cand) {
+            const unsigned tb = (unsigned)(((long long)g.LB * g.T + 255) / 256);
+            k_topk_select<__nv_bfloat16><<<tb, 256, 0, s>>>(
                 (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
                 pool->pool_size, cand, xnorm, rn_max, g.LB, g.T, g.W, g.n_ref, g.k,
                 g.max_chunks, (int4 *)ref_idx, copy_flag, scan_list, scan_count);
+        } else if (ref_exact_is_f32) {
+            k_topk_scan_warp<float><<<blocks, 256, 0, s>>>(
+                (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size,
+                g.LB, g.T, g.W, g.n_ref, g.k, (int4 *)ref_idx, copy_flag);
+        } else {
+            k_topk_scan_warp<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
+                pool->pool_size, g.LB, g.T, g.W, g.n_ref, g.k, (int4 *)ref_idx, copy_flag);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (scan_list) {

@@ -35,8 +35,9 @@ constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kMergeBytes = 8 * 1024;        // S1: per-warp token info
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kMergeBytes;
+constexpr int kInfoBytes = kEpiWarps * 64 * 32; // S1: 64 tokens x 32 B per epilogue warp
+constexpr int kS1Round = 8;                     // S1: tokens whose gathers are in flight at once
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kInfoBytes;
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
 // projections run transposed: D[f][t] = W[f][:] . X[t][:], two 128x128 MMAs per step
 constexpr uint32_t kIdescT = um::idesc_bf16_f32(kBM, kBN / 2);
@@ -320,6 +321,40 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             }
             bool is_ref = true;
             if (MODE == M_S2) is_ref = in ? (a.ref_slot[r] >= 0) : true;
+            if (MODE == M_S1) {
+                // this warp's 64 tokens: row offsets of the chosen references' projection
+                // rows (unused places point at the all-zero row), 1/k and a live flag,
+                // prepared in shared memory while the accumulator fills
+                int4 *info = info_buf + (warp - 2) * 128;
+                const int zoff = a.LB * a.n_ref * a.d_ff;
+                const int lboff = it.lb * a.n_ref;
+                __syncwarp();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int tj = it.m * kBM + h * 64 + cc * 32 + lane;
+                    int rs = 0, cf = 1;
+                    int4 ix = make_int4(-1, -1, -1, -1);
+                    if (tj < a.rows) {
+                        rs = a.ref_slot[tj];
+                        cf = a.copy_flag[(size_t)it.lb * a.T + tj];
+                        ix = a.ref_idx[(size_t)it.lb * a.T + tj];
+                    }
+                    int4 o = make_int4(zoff, zoff, zoff, zoff);
+                    float inv_k = 0.0f, live = 0.0f;
+                    if (rs < 0 && !cf) {
+                        int kk = 0;
+                        if (ix.x >= 0) { o.x = (lboff + ix.x) * a.d_ff; ++kk; }
+                        if (ix.y >= 0) { o.y = (lboff + ix.y) * a.d_ff; ++kk; }
+                        if (ix.z >= 0) { o.z = (lboff + ix.z) * a.d_ff; ++kk; }
+                        if (ix.w >= 0) { o.w = (lboff + ix.w) * a.d_ff; ++kk; }
+                        inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
+                        live = 1.0f;
+                    }
+                    info[2 * (cc * 32 + lane)] = o;
+                    info[2 * (cc * 32 + lane) + 1] = make_int4(__float_as_int(inv_k), __float_as_int(live), 0, 0);
+                }
+                __syncwarp();
+            }
 
             for (int n = it.n0; n < it.n1; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
@@ -382,70 +417,46 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                 } else if (MODE == M_S1) {
                     // lane = d_ff column f, TMEM column = token.  For each token the
-                    // warp reads its references' projection rows as 128-byte lines.
-                    // Lane j first prepares token j's 32-bit row offsets (unused slots
-                    // point at the all-zero row), 1/k and a live flag in shared memory.
+                    // warp reads its references' projection rows as 128-byte lines,
+                    // kS1Round tokens (8 loads each) in flight per round.
                     const int f = n * (kBN / 2) + q * 32 + lane;
                     const bool fok = f < a.d_ff;
                     const float *P1f = a.P1 + (fok ? f : 0);
                     const float *P2f = a.P2 + (fok ? f : 0);
-                    int4 *info = info_buf + (warp - 2) * 64;   // 32 tokens x 2 int4
-                    const int zoff = a.LB * a.n_ref * a.d_ff;
-                    const int lboff = it.lb * a.n_ref;
+                    const int4 *info = info_buf + (warp - 2) * 128;
 #pragma unroll 1
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c0 = h * 64 + cc * 32;
-                        float v1[32], v2[32];
-                        um::tmem_ld32(tb + c0, v1);
-                        um::tmem_ld32(tb + kBN / 2 + c0, v2);
-                        const int t0 = it.m * kBM + c0;
-                        {
-                            const int tj = t0 + lane;
-                            int4 o = make_int4(zoff, zoff, zoff, zoff);
-                            float inv_k = 0.0f, live = 0.0f;
-                            if (tj < a.rows && a.ref_slot[tj] < 0 && !a.copy_flag[(size_t)it.lb * a.T + tj]) {
-                                const int4 ix = a.ref_idx[(size_t)it.lb * a.T + tj];
-                                int kk = 0;
-                                if (ix.x >= 0) { o.x = (lboff + ix.x) * a.d_ff; ++kk; }
-                                if (ix.y >= 0) { o.y = (lboff + ix.y) * a.d_ff; ++kk; }
-                                if (ix.z >= 0) { o.z = (lboff + ix.z) * a.d_ff; ++kk; }
-                                if (ix.w >= 0) { o.w = (lboff + ix.w) * a.d_ff; ++kk; }
-                                inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
-                                live = 1.0f;
-                            }
-                            __syncwarp();
-                            info[2 * lane] = o;
-                            info[2 * lane + 1] = make_int4(__float_as_int(inv_k), __float_as_int(live), 0, 0);
-                            __syncwarp();
+                    for (int c = 0; c < 64; c += kS1Round) {
+                        const int t0 = it.m * kBM + h * 64 + c;
+                        float x1[kS1Round][4], x2[kS1Round][4], ik[kS1Round], lv[kS1Round];
+#pragma unroll
+                        for (int u = 0; u < kS1Round; ++u) {
+                            const int4 o = info[2 * (c + u)];
+                            const int4 b = info[2 * (c + u) + 1];
+                            ik[u] = __int_as_float(b.x);
+                            lv[u] = __int_as_float(b.y);
+                            x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
+                            x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
+                            x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
+                            x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
+                        }
+                        float v1[kS1Round], v2[kS1Round];
+#pragma unroll
+                        for (int p8 = 0; p8 < kS1Round; p8 += 8) {
+                            um::tmem_ld8(tb + h * 64 + c + p8, v1 + p8);
+                            um::tmem_ld8(tb + kBN / 2 + h * 64 + c + p8, v2 + p8);
                         }
                         __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
                         __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
 #pragma unroll
-                        for (int j0 = 0; j0 < 32; j0 += 4) {
-                            float x1[4][4], x2[4][4], ik[4], lv[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int4 o = info[2 * (j0 + u)];
-                                const int4 b = info[2 * (j0 + u) + 1];
-                                ik[u] = __int_as_float(b.x);
-                                lv[u] = __int_as_float(b.y);
-                                x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
-                                x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
-                                x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
-                                x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
-                            }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int j = j0 + u;
-                                const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
-                                const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
-                                // reference token or exact copy: lv = 0, z = 0
-                                const float dh = (silu_fast(v1[j]) * v2[j] - silu_fast(m1) * m2) * lv[u];
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
-                                if (fok && t0 + j < a.rows) {
-                                    hi[(size_t)j * a.d_ff] = hb;
-                                    lo[(size_t)j * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
-                                }
+                        for (int u = 0; u < kS1Round; ++u) {
+                            const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
+                            const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
+                            // reference token or exact copy: lv = 0, z = 0
+                            const float dh = (silu_fast(v1[u]) * v2[u] - silu_fast(m1) * m2) * lv[u];
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
+                            if (fok && t0 + u < a.rows) {
+                                hi[(size_t)u * a.d_ff] = hb;
+                                lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
                             }
                         }
                     }
