@@ -46,7 +46,7 @@ Geometry make_geometry(const rkv_params *p)
     g.first = p->first;
     g.alpha = p->alpha;
     g.n_sink = p->n_sink;
-    g.n_mtiles = (p->T + kBM - 1) / kBM;
+    g.n_mtiles = (p->T + kTileM - 1) / kTileM;
     int max_nt = (g.n_ref + kBN - 1) / kBN;
     g.max_chunks = max_nt == 0 ? 1 : (max_nt + kDistChunk - 1) / kDistChunk;
     return g;

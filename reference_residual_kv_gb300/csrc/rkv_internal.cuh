@@ -29,6 +29,7 @@ constexpr int kMaxK = 4;                  // ref_idx rows are int4
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
+constexpr int kTileM = 2 * kBM;          // token rows of a CTA-pair tile (2-SM MMA, M = 256)
 constexpr int kDistChunk = 8;             // N-tiles (2048 references) per distance work item
 
 // Bounded waits: ~1 s at 2 GHz.
@@ -39,7 +40,7 @@ struct Geometry {
     int kv_dtype, ref_dtype;
     int stride, first, n_sink;
     double alpha;
-    int n_mtiles;        // ceil(T / 128)
+    int n_mtiles;        // ceil(T / kTileM): CTA-pair token tiles
     int max_chunks;      // distance work items per token tile
 };
 
@@ -109,10 +110,10 @@ __device__ __forceinline__ void set_status(int32_t *st, int code)
     if (st) atomicCAS(st, 0, code);
 }
 
-// Number of N-tiles (256 references) a 128-token tile needs: its last row's pool.
+// Number of N-tiles (256 references) the 256-token pair tile m needs: its last row's pool.
 __device__ __forceinline__ int dist_ntiles(const int32_t *pool_size, int T, int m)
 {
-    int last = min(T, (m + 1) * kBM) - 1;
+    int last = min(T, (m + 1) * kTileM) - 1;
     int pool = pool_size[last];
     return (pool + kBN - 1) / kBN;
 }

@@ -208,7 +208,7 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
             for (int j = 0; j < kMaxK; ++j) ch[j] = j < pool ? j : kNoSlot;
             state = pool > 0 ? kCopyCheck : kDone;
         } else {
-            const int nch = (dist_ntiles(pool_size, T_, t / kBM) + kDistChunk - 1) / kDistChunk;
+            const int nch = (dist_ntiles(pool_size, T_, t / kTileM) + kDistChunk - 1) / kDistChunk;
             nlists = 2 * nch;
             const float4 *cp = (const float4 *)(cand + (size_t)gt * max_chunks * kCand);
             float te[kMaxK + 1];

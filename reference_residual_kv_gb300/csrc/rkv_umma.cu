@@ -1,15 +1,18 @@
 // rkv_umma.cu -- the write path for bf16 kv on the 5th-generation tensor cores.
 //
 // All four dense contractions of the path run through one persistent,
-// warp-specialised kernel (one CTA per SM):
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 4 stages
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, bf16 -> fp32,
-//               into one of two 256-column TMEM accumulators
-//   warps 2..9  epilogue: one accumulator row (= one token or reference) per
-//               thread and half of the columns per warp, read with tcgen05.ld
-//               while the next tile accumulates
+// warp-specialised kernel launched as CTA pairs (clusters of 2) that issue 2-SM
+// MMAs: tcgen05.mma.cta_group::2, 256 x 256 x 16, bf16 in, fp32 in TMEM.  Each CTA
+// of a pair holds 128 rows of A and half (128 rows) of B in its own shared memory;
+// the leader (rank 0) issues the MMAs and each CTA's TMEM receives its own 128 rows
+// of the 256 x 256 product, so each SM reads 8 KB of operands per 1 MFLOP step
+// (a single-SM 128 x 128 step reads the same 8 KB for half the work).
+//   warp 0      TMA producer (both CTAs): this CTA's A rows and B half per stage
+//   warp 1      TMEM allocation (both CTAs, 512 columns = two 256-column
+//               accumulators); MMA issue (leader only)
+//   warps 2..9  epilogue: TMEM lane quarter q = warp % 4, column half h
 // The epilogue is what differs between the four uses:
-//   M_P    P1 | P2 = R [W_c1 | W_c2] for each stored reference (fp32 out)
+//   M_P    P1 | P2 = R W_c1^T | R W_c2^T for each stored reference (fp32 out)
 //   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kList per row
 //          and column half
 //          [RKV §2.2 = Sec. IV-A; ||x||^2 is common to a row and left out]
@@ -18,6 +21,11 @@
 //          by linearity [RKV §2.2, §2.3 = Sec. IV-A]; stored as bf16 hi + lo
 //   M_S2   z = dh_hi W_c3 + dh_lo W_c3 = f_c(kv) - f_c(mean), then per-token
 //          group min/max quantisation and packing [RKV §2.4]
+// M_P and M_S1 run transposed (weights on the MMA's M side, tokens on N): each CTA's
+// 128 A rows are 64 rows of W_c1 and the same 64 rows of W_c2, so TMEM lane l < 64
+// holds x.W_c1[f] and lane 64 + l holds x.W_c2[f] of one d_ff column f, and a warp's
+// 32 lanes are 32 consecutive f: the epilogue's per-token gathers of reference
+// projections and its stores are 128-byte lines.
 // Every mbarrier wait is bounded; on expiry the kernel reports
 // RKV_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and returns.
 #include "rkv_internal.cuh"
@@ -29,28 +37,32 @@ namespace rkv {
 
 enum { M_P = 0, M_DIST = 1, M_S1 = 2, M_S2 = 3 };
 
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kHalfN = kBN / 2;                  // B rows each CTA of a pair holds
+constexpr int kABytes = kBM * kBK * 2;           // 16 KB
+constexpr int kBBytes = kHalfN * kBK * 2;        // 16 KB
+constexpr int kStageBytes = kABytes + kBBytes;   // per CTA
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kInfoBytes = kEpiWarps * 64 * 32; // S1: 64 tokens x 32 B per epilogue warp
-constexpr int kS1Round = 8;                     // S1: tokens whose gathers are in flight at once
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kInfoBytes;
-constexpr uint32_t kIdesc = um::idesc_bf16_f32(kBM, kBN);
-// projections run transposed: D[f][t] = W[f][:] . X[t][:], two 128x128 MMAs per step
-constexpr uint32_t kIdescT = um::idesc_bf16_f32(kBM, kBN / 2);
+constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epilogue warp
+constexpr int kS1Round = 8;                      // S1: tokens whose gathers are in flight at once
+constexpr int kXTok = 16;                        // S1: tokens per exchange between warp pairs
+constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
+constexpr uint32_t kIdesc = um::idesc_bf16_f32(2 * kBM, kBN);
+constexpr uint16_t kPairMask = 3;
 
-// M_P and M_S1 put the weights on the MMA's M side (TMEM lane = d_ff column f) and
-// the tokens (or references) on N (TMEM column = token), so that the epilogue's
-// per-token gathers of reference projections and its stores are coalesced across
-// the 32 lanes of a warp (consecutive f).
-template <int MODE> struct Transposed { static constexpr bool value = MODE == M_P || MODE == M_S1; };
+template <int MODE> struct Cfg {
+    static constexpr bool kT = MODE == M_P || MODE == M_S1;   // transposed
+    static constexpr int kStages = MODE == M_S1 ? 5 : 6;
+    static constexpr int kExtra = MODE == M_S1 ? kInfoBytes + kXBytes : 0;
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256 + kExtra;
+};
 
 struct UmmaArgs {
-    int LB, B, T, rows;   // rows: A-operand rows per lb (T, or n_ref for M_P)
-    int n_mtiles, n_ntiles, k_chunks, a_sources, b_split, b_per_layer, max_chunks;
+    int LB, B, T, rows;   // rows: token (reference for M_P) rows per lb
+    int tiles_t;          // ceil(rows / 256): pair tiles of tokens (references)
+    int tiles_n;          // M_P/M_S1: 128-column d_ff slices; M_S2: 256-column d_c tiles;
+                          // M_DIST: distance chunks (max_chunks)
+    int k_chunks, a_sources;
     int W, d_ff, d_c, n_ref, bits;
     float *P1, *P2;
     const float *ref_sqnorm;
@@ -65,52 +77,36 @@ struct UmmaArgs {
     int32_t *status;
 };
 
-struct Item { int lb, m, n0, n1, chunk; };
+// One work item of a pair: (lb, token tile t of 256 rows, N range [n0, n1)).
+struct Item { int lb, t, n0, n1, chunk; };
 
-// A cluster of C CTAs works on C consecutive token tiles against the same B tiles
-// (weights or references), each CTA loading 1/C of every B tile and multicasting it
-// to all C.
-template <int C>
-__device__ __forceinline__ int n_groups(const UmmaArgs &a) { return (a.n_mtiles + C - 1) / C; }
-
-template <int MODE, int C>
 __device__ __forceinline__ int item_count(const UmmaArgs &a)
 {
-    return a.LB * n_groups<C>(a) * (MODE == M_DIST ? a.max_chunks : a.n_ntiles);
+    return a.LB * a.tiles_t * a.tiles_n;
 }
 
-// Work item i -> (lb, this CTA's token tile, N-tile range), identical N range and K
-// loop for all CTAs of the cluster.  The (layer, sequence) index is the slowest, so
-// the CTAs in flight share one layer's weights, references and projections in L2;
-// the N tile is the fastest, so neighbouring CTAs reuse the same token rows.
-// Distance items visit the late (largest-pool) token tiles first; a group's N range
-// is that of its last tile.
-template <int MODE, int C>
-__device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, int rank, Item &it)
+// The (layer, sequence) index is the slowest, so the pairs in flight share one layer's
+// weights, references and projections in L2; the N index is the fastest, so
+// neighbouring pairs reuse the same token rows.  Distance items visit the late
+// (largest-pool) token tiles first.
+template <int MODE>
+__device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, Item &it)
 {
-    const int ng = n_groups<C>(a);
+    const int n = i % a.tiles_n, r = i / a.tiles_n;
+    it.lb = r / a.tiles_t;
+    it.t = r % a.tiles_t;
+    it.chunk = 0;
     if (MODE == M_DIST) {
-        const int chunk = i % a.max_chunks, r = i / a.max_chunks;
-        const int g = ng - 1 - r % ng, lb = r / ng;
-        const int last = min(a.n_mtiles - 1, g * C + C - 1);
-        const int nt = dist_ntiles(a.pool_size, a.T, last);
-        it.lb = lb; it.m = g * C + rank; it.chunk = chunk;
-        it.n0 = chunk * kDistChunk;
+        it.t = a.tiles_t - 1 - it.t;
+        const int nt = dist_ntiles(a.pool_size, a.T, it.t);
+        it.chunk = n;
+        it.n0 = n * kDistChunk;
         it.n1 = min(nt, it.n0 + kDistChunk);
         return it.n0 < it.n1;
     }
-    const int n = i % a.n_ntiles, r = i / a.n_ntiles;
-    it.m = (r % ng) * C + rank; it.lb = r / ng; it.chunk = 0;
-    it.n0 = n; it.n1 = n + 1;
+    it.n0 = n;
+    it.n1 = n + 1;
     return true;
-}
-
-__device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float (&v)[8])
-{
-    __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
-    *(uint4 *)dst = *(const uint4 *)o;
 }
 
 // Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
@@ -119,51 +115,51 @@ __device__ __forceinline__ float silu_fast(float u)
     return __fdividef(u, 1.0f + __expf(-u));
 }
 
-template <int MODE, int C>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-       const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-       const UmmaArgs a)
+       const __grid_constant__ CUtensorMap tmB, const UmmaArgs a)
 {
+    using C = Cfg<MODE>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = smem_raw + ((1024u - (um::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = (uint64_t *)(tiles + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *tfull = empty + kStages;
-    uint64_t *tempty = tfull + 2;
+    uint64_t *full = (uint64_t *)(tiles + S * kStageBytes);   // leader's: both CTAs' bytes
+    uint64_t *empty = full + S;                                  // freed by the pair's MMA
+    uint64_t *tfull = empty + S;
+    uint64_t *tempty = tfull + 2;                                // leader's: both epilogues
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
-    int4 *info_buf = (int4 *)(tiles + kStages * kStageBytes + 256);
+    int4 *info_buf = (int4 *)(tiles + S * kStageBytes + 256);
+    float *xbuf = (float *)(tiles + S * kStageBytes + 256 + kInfoBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = um::cluster_rank();
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             um::mbar_init(&full[s], 1);
-            um::mbar_init(&empty[s], C);          // one commit from every CTA of the cluster
+            um::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             um::mbar_init(&tfull[b], 1);
-            um::mbar_init(&tempty[b], 32 * kEpiWarps);
+            um::mbar_init(&tempty[b], 2 * kEpiWarps);
         }
         um::mbar_init(drain, 1);
         *abort_flag = 0;
         um::fence_mbar_init();
     }
     if (warp == 1) {
-        um::tmem_alloc(tmem_slot, 512);
-        um::tmem_relinquish();
+        um::tmem_alloc2(tmem_slot, 512);
+        um::tmem_relinquish2();
     }
     um::tc_fence_before();
-    if (C > 1) um::cluster_sync();   // peers multicast into our stages only after our init
-    else __syncthreads();
+    um::cluster_sync();   // the peer signals our barriers only after our init
     um::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = item_count<MODE, C>(a);
-    const int rank = C > 1 ? (int)um::cluster_rank() : 0;
-    const int cid = blockIdx.x / C, ncl = gridDim.x / C;
-    constexpr uint16_t kMask = (uint16_t)((1u << C) - 1u);
-    constexpr int kSlice = kBN / C;                // B rows each CTA loads
+    const int n_items = item_count(a);
+    const int pid = blockIdx.x / 2, npairs = gridDim.x / 2;
     const int k_iters = a.k_chunks * a.a_sources;
 
     if (warp == 0) {
@@ -171,52 +167,48 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         if (lane == 0) {
             um::prefetch_tmap(&tmA0);
             um::prefetch_tmap(&tmA1);
-            um::prefetch_tmap(&tmB0);
-            um::prefetch_tmap(&tmB1);
+            um::prefetch_tmap(&tmB);
             int stage = 0;
             uint32_t ph = 0;
-            uint32_t last_ph[kStages];
-            bool used[kStages];
-            for (int s = 0; s < kStages; ++s) { used[s] = false; last_ph[s] = 0; }
+            uint32_t last_ph[S];
+            bool used[S];
+            for (int s = 0; s < S; ++s) { used[s] = false; last_ph[s] = 0; }
             bool ok = true;
-            for (int i = cid; i < n_items && ok; i += ncl) {
+            for (int i = pid; i < n_items && ok; i += npairs) {
                 Item it;
-                if (!item_get<MODE, C>(a, i, rank, it)) continue;
-                const int bz = a.b_per_layer ? it.lb / a.B : it.lb;
+                if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     for (int kc = 0; kc < k_iters; ++kc) {
-                        if (*abort_flag || !um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles)) {
+                        const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles);
+                        if (*abort_flag || !w) {
                             ok = false;
                             break;
                         }
                         uint8_t *sa = tiles + stage * kStageBytes;
                         uint8_t *sb = sa + kABytes;
-                        um::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                        const uint32_t fb = um::smem_u32(&full[stage]);
+                        // the leader's full barrier counts both CTAs' bytes
+                        if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                        const uint32_t bar = leader ? fb : um::mapa(fb, 0);
                         const int src = kc / a.k_chunks;
                         const int kx = (kc - src * a.k_chunks) * kBK;
-                        um::tma_load_3d(sa, src ? &tmA1 : &tmA0, &full[stage], kx, it.m * kBM, it.lb);
-                        if (C == 1) {
-                            if (a.b_split) {
-                                um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * (kBN / 2), bz);
-                                um::tma_load_3d(sb + kBBytes / 2, &tmB1, &full[stage], kx, n * (kBN / 2), bz);
-                            } else {
-                                um::tma_load_3d(sb, &tmB0, &full[stage], kx, n * kBN, bz);
-                            }
+                        if (C::kT) {
+                            // A: 64 rows of W_c1 and the same 64 rows of W_c2; B: 128 tokens
+                            const int f0 = n * kBM + (int)rank * (kBM / 2);
+                            const int lz = it.lb / a.B;
+                            um::tma_load_3d_pair(sa, &tmA0, bar, kx, f0, lz);
+                            um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, f0, lz);
+                            um::tma_load_3d_pair(sb, &tmB, bar, kx, it.t * 2 * kBM + (int)rank * kBM, it.lb);
                         } else {
-                            // this CTA's slice of the B tile, into every CTA of the cluster;
-                            // split B: slices [0, C/2) from tmB0, [C/2, C) from tmB1
-                            uint8_t *dst = sb + rank * kSlice * (kBK * 2);
-                            if (a.b_split) {
-                                const int hs = C / 2;
-                                const int yrow = n * (kBN / 2) + (rank % hs) * kSlice;
-                                um::tma_load_3d_mc(dst, rank < hs ? &tmB0 : &tmB1, &full[stage], kx, yrow, bz, kMask);
-                            } else {
-                                um::tma_load_3d_mc(dst, &tmB0, &full[stage], kx, n * kBN + rank * kSlice, bz, kMask);
-                            }
+                            // A: 128 token rows (M_S2: dh_hi, then dh_lo); B: half of N tile n
+                            um::tma_load_3d_pair(sa, src ? &tmA1 : &tmA0, bar, kx,
+                                                 it.t * 2 * kBM + (int)rank * kBM, it.lb);
+                            um::tma_load_3d_pair(sb, &tmB, bar, kx, n * kBN + (int)rank * kHalfN,
+                                                 MODE == M_S2 ? it.lb / a.B : it.lb);
                         }
                         used[stage] = true;
                         last_ph[stage] = ph;
-                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                        if (++stage == S) { stage = 0; ph ^= 1u; }
                     }
                 }
             }
@@ -224,39 +216,31 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
             }
-            // every issued copy must land before the CTA may exit
-            for (int s = 0; s < kStages; ++s)
-                if (used[s]) um::mbar_wait(&full[s], last_ph[s], kWaitCycles);
+            // a stage's copies have landed once the pair's MMA has freed it
+            for (int s = 0; s < S; ++s)
+                if (used[s]) um::mbar_wait(&empty[s], last_ph[s], kWaitCycles);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (leader && lane == 0) {
             int stage = 0;
             uint32_t ph = 0, cnt = 0;
             bool ok = true;
-            for (int i = cid; i < n_items && ok; i += ncl) {
+            for (int i = pid; i < n_items && ok; i += npairs) {
                 Item it;
-                if (!item_get<MODE, C>(a, i, rank, it)) continue;
+                if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
-                    if (*abort_flag || !um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles)) {
+                    const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles);
+                    if (*abort_flag || !w) {
                         ok = false;
                         break;
                     }
                     um::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
-                    // distance tiles: only the references this CTA's token rows can see
-                    // (causal pool of its last row), N rounded up to 16; none -> no MMA
-                    uint32_t idesc = kIdesc;
-                    bool issue = true;
-                    if (MODE == M_DIST) {
-                        const int own = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1] - n * kBN;
-                        const int cols = own < kBN ? own : kBN;
-                        issue = it.m < a.n_mtiles && cols > 0;
-                        if (issue) idesc = um::idesc_bf16_f32(kBM, (cols + 15) & ~15);
-                    }
                     for (int kc = 0; kc < k_iters; ++kc) {
-                        if (*abort_flag || !um::mbar_wait(&full[stage], ph, kWaitCycles)) {
+                        const bool wf = um::mbar_wait(&full[stage], ph, kWaitCycles);
+                        if (*abort_flag || !wf) {
                             ok = false;
                             break;
                         }
@@ -264,25 +248,14 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const uint32_t sa = um::smem_u32(tiles + stage * kStageBytes);
                         const uint64_t ad = um::sdesc_sw128(sa);
                         const uint64_t bd = um::sdesc_sw128(sa + kABytes);
-                        if (Transposed<MODE>::value) {
-                            // stage = [token tile | W1 tile | W2 tile]: D1 = W1 X^T, D2 = W2 X^T
-                            const uint64_t w1 = bd, w2 = um::sdesc_sw128(sa + kABytes + kBBytes / 2);
 #pragma unroll
-                            for (int k = 0; k < kBK / 16; ++k) {
-                                um::mma_bf16(d_tmem, w1 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
-                                um::mma_bf16(d_tmem + kBN / 2, w2 + 2 * k, ad + 2 * k, kIdescT, (kc | k) != 0);
-                            }
-                        } else if (issue) {
-#pragma unroll
-                            for (int k = 0; k < kBK / 16; ++k)
-                                um::mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
-                        }
-                        if (C > 1) um::mma_commit_mc(&empty[stage], kMask);
-                        else um::mma_commit(&empty[stage]);
-                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                        for (int k = 0; k < kBK / 16; ++k)
+                            um::mma2_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                        um::mma2_commit_mc(&empty[stage], kPairMask);
+                        if (++stage == S) { stage = 0; ph ^= 1u; }
                     }
                     if (!ok) break;
-                    um::mma_commit(&tfull[buf]);
+                    um::mma2_commit_mc(&tfull[buf], kPairMask);
                     ++cnt;
                 }
             }
@@ -291,7 +264,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 *abort_flag = 1;
             }
             // all issued MMAs complete before TMEM can be released
-            um::mma_commit(drain);
+            um::mma2_commit_mc(drain, 1);
             um::mbar_wait(drain, 0, kWaitCycles);
         }
     } else {
@@ -302,12 +275,15 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         const int h = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-        uint32_t cnt = 0;
+        // M_S1: warps (q, h) and (q ^ 2, h) hold the two gate halves of the same
+        // 32 d_ff columns and trade accumulator columns through shared memory
+        const int pair_id = 1 + (q & 1) + 2 * h;
+        uint32_t cnt = 0, xcnt = 0;
         bool ok = true;
-        for (int i = cid; i < n_items; i += ncl) {
+        for (int i = pid; i < n_items; i += npairs) {
             Item it;
-            if (!item_get<MODE, C>(a, i, rank, it)) continue;
-            const int r = it.m * kBM + row;
+            if (!item_get<MODE>(a, i, it)) continue;
+            const int r = it.t * 2 * kBM + (int)rank * kBM + row;   // token row (M_DIST, M_S2)
             const bool in = r < a.rows;
 
             float be[kList];
@@ -317,7 +293,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
                 for (int j = 0; j < kList; ++j) { be[j] = INFINITY; bs[j] = -1; }
                 pool = in ? a.pool_size[r] : 0;
-                tile_pool = a.pool_size[min(a.T, (it.m + 1) * kBM) - 1];
+                tile_pool = a.pool_size[min(a.T, (it.t + 1) * 2 * kBM) - 1];
             }
             bool is_ref = true;
             if (MODE == M_S2) is_ref = in ? (a.ref_slot[r] >= 0) : true;
@@ -326,12 +302,13 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 // rows (unused places point at the all-zero row), 1/k and a live flag,
                 // prepared in shared memory while the accumulator fills
                 int4 *info = info_buf + (warp - 2) * 128;
+                const int own0 = h * kHalfN + (q < 2 ? 0 : 64);
                 const int zoff = a.LB * a.n_ref * a.d_ff;
                 const int lboff = it.lb * a.n_ref;
                 __syncwarp();
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    const int tj = it.m * kBM + h * 64 + cc * 32 + lane;
+                    const int tj = it.t * 2 * kBM + own0 + cc * 32 + lane;
                     int rs = 0, cf = 1;
                     int4 ix = make_int4(-1, -1, -1, -1);
                     if (tj < a.rows) {
@@ -359,36 +336,32 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             for (int n = it.n0; n < it.n1; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
                 bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                w = __all_sync(0xffffffffu, w);
+                if (MODE == M_S1) w = um::bar_and(pair_id, 64, w);   // the pair leaves together
+                if (!w) { ok = false; break; }
                 um::tc_fence_after();
                 const uint32_t tb = tl + buf * kBN;
 
                 if (MODE == M_P) {
-                    // lane = d_ff column f, TMEM column = reference slot
-                    const int f = n * (kBN / 2) + q * 32 + lane;
+                    // lane = d_ff column f of W_c1 (q < 2) or W_c2, TMEM column = reference
+                    const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
+                    float *P = (q < 2 ? a.P1 : a.P2) + (size_t)it.lb * a.n_ref * a.d_ff + f;
 #pragma unroll 1
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c0 = h * 64 + cc * 32;
-                        float v1[32], v2[32];
-                        um::tmem_ld32(tb + c0, v1);
-                        um::tmem_ld32(tb + kBN / 2 + c0, v2);
-                        const int r0 = it.m * kBM + c0;
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c0 = h * kHalfN + cc * 32;
+                        float v[32];
+                        um::tmem_ld32(tb + c0, v);
+                        const int r0 = it.t * 2 * kBM + c0;
                         if (f < a.d_ff) {
-                            float *p1 = a.P1 + ((size_t)it.lb * a.n_ref + r0) * a.d_ff + f;
-                            float *p2 = a.P2 + ((size_t)it.lb * a.n_ref + r0) * a.d_ff + f;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                if (r0 + j < a.rows) {
-                                    p1[(size_t)j * a.d_ff] = v1[j];
-                                    p2[(size_t)j * a.d_ff] = v2[j];
-                                }
-                            }
+                            for (int j = 0; j < 32; ++j)
+                                if (r0 + j < a.rows) P[(size_t)(r0 + j) * a.d_ff] = v[j];
                         }
                     }
                 } else if (MODE == M_DIST) {
                     const float *rn = a.ref_sqnorm + (size_t)it.lb * a.n_ref;
 #pragma unroll 1
-                    for (int c0 = h * (kBN / 2); c0 < (h + 1) * (kBN / 2); c0 += 32) {
+                    for (int c0 = h * kHalfN; c0 < (h + 1) * kHalfN; c0 += 32) {
                         const int s0 = n * kBN + c0;
                         if (s0 >= tile_pool) break;          // uniform over the warp
                         float v[32];
@@ -416,47 +389,67 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 } else if (MODE == M_S1) {
-                    // lane = d_ff column f, TMEM column = token.  For each token the
-                    // warp reads its references' projection rows as 128-byte lines,
-                    // kS1Round tokens (8 loads each) in flight per round.
-                    const int f = n * (kBN / 2) + q * 32 + lane;
+                    // lane = d_ff column f; this warp holds x.W_c1[f] (q < 2) or x.W_c2[f]
+                    // for all 256 tokens of the tile, finishes 64 of them and hands the
+                    // other gate half of its partner's 64 over
+                    const bool gate = q < 2;
+                    const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
                     const bool fok = f < a.d_ff;
                     const float *P1f = a.P1 + (fok ? f : 0);
                     const float *P2f = a.P2 + (fok ? f : 0);
+                    const int own0 = h * kHalfN + (gate ? 0 : 64);
+                    const int give0 = h * kHalfN + (gate ? 64 : 0);
                     const int4 *info = info_buf + (warp - 2) * 128;
+                    const int gb = 2 + 4 * h;                     // first warp of this half
+                    const int me = warp - 2, partner = gb + ((warp - gb) ^ 2) - 2;
 #pragma unroll 1
-                    for (int c = 0; c < 64; c += kS1Round) {
-                        const int t0 = it.m * kBM + h * 64 + c;
-                        float x1[kS1Round][4], x2[kS1Round][4], ik[kS1Round], lv[kS1Round];
+                    for (int c = 0; c < 64; c += kXTok) {
+                        // double-buffered: a buffer is rewritten only after the next
+                        // exchange barrier, which the partner reaches after reading it
+                        float *xw = xbuf + (size_t)(((xcnt & 1u) * kEpiWarps + me) * kXTok) * 32;
+                        const float *xr = xbuf + (size_t)(((xcnt & 1u) * kEpiWarps + partner) * kXTok) * 32;
+                        ++xcnt;
 #pragma unroll
-                        for (int u = 0; u < kS1Round; ++u) {
-                            const int4 o = info[2 * (c + u)];
-                            const int4 b = info[2 * (c + u) + 1];
-                            ik[u] = __int_as_float(b.x);
-                            lv[u] = __int_as_float(b.y);
-                            x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
-                            x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
-                            x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
-                            x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
+                        for (int p8 = 0; p8 < kXTok; p8 += 8) {
+                            float g[8];
+                            um::tmem_ld8(tb + give0 + c + p8, g);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) xw[(p8 + j) * 32 + lane] = g[j];
                         }
-                        float v1[kS1Round], v2[kS1Round];
+                        um::bar_sync(pair_id, 64);
+#pragma unroll 1
+                        for (int r8 = 0; r8 < kXTok; r8 += kS1Round) {
+                            const int cc = c + r8;
+                            float x1[kS1Round][4], x2[kS1Round][4], ik[kS1Round], lv[kS1Round];
 #pragma unroll
-                        for (int p8 = 0; p8 < kS1Round; p8 += 8) {
-                            um::tmem_ld8(tb + h * 64 + c + p8, v1 + p8);
-                            um::tmem_ld8(tb + kBN / 2 + h * 64 + c + p8, v2 + p8);
-                        }
-                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
-                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+                            for (int u = 0; u < kS1Round; ++u) {
+                                const int4 o = info[2 * (cc + u)];
+                                const int4 b = info[2 * (cc + u) + 1];
+                                ik[u] = __int_as_float(b.x);
+                                lv[u] = __int_as_float(b.y);
+                                x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
+                                x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
+                                x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
+                                x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
+                            }
+                            float v[kS1Round];
+                            um::tmem_ld8(tb + own0 + cc, v);
+                            const int t0 = it.t * 2 * kBM + own0 + cc;
+                            __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+                            __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
 #pragma unroll
-                        for (int u = 0; u < kS1Round; ++u) {
-                            const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
-                            const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
-                            // reference token or exact copy: lv = 0, z = 0
-                            const float dh = (silu_fast(v1[u]) * v2[u] - silu_fast(m1) * m2) * lv[u];
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
-                            if (fok && t0 + u < a.rows) {
-                                hi[(size_t)u * a.d_ff] = hb;
-                                lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                            for (int u = 0; u < kS1Round; ++u) {
+                                const float pv = xr[(r8 + u) * 32 + lane];
+                                const float g1 = gate ? v[u] : pv, g2 = gate ? pv : v[u];
+                                const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
+                                const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
+                                // reference token or exact copy: lv = 0, z = 0
+                                const float dh = (silu_fast(g1) * g2 - silu_fast(m1) * m2) * lv[u];
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
+                                if (fok && t0 + u < a.rows) {
+                                    hi[(size_t)u * a.d_ff] = hb;
+                                    lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                                }
                             }
                         }
                     }
@@ -489,14 +482,20 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 }
+                // this warp is done with the accumulator: one arrival on the leader's
+                // barrier (which counts both CTAs' epilogue warps)
                 um::tc_fence_before();
-                um::mbar_arrive(&tempty[buf]);
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) um::mbar_arrive(&tempty[buf]);
+                    else um::mbar_arrive_cluster(um::mapa(um::smem_u32(&tempty[buf]), 0));
+                }
                 ++cnt;
             }
             if (MODE == M_DIST && ok && in) {
                 // this warp's sorted list (its half of the columns) as is; the two
                 // halves' lists stay separate: [chunk][h * kList + j]
-                float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.max_chunks + it.chunk) * kCand +
+                float4 *cp = (float4 *)(a.cand + (((size_t)it.lb * a.T + r) * a.tiles_n + it.chunk) * kCand +
                                         h * kList);
 #pragma unroll
                 for (int j = 0; j < kList / 2; ++j)
@@ -512,12 +511,12 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     }
 
     um::tc_fence_before();
-    // no CTA leaves while a peer may still multicast into it or signal its barriers
-    if (C > 1) um::cluster_sync();
-    else __syncthreads();
+    // no CTA leaves while its peer may still read its shared memory or signal its
+    // barriers
+    um::cluster_sync();
     if (warp == 1) {
         um::tc_fence_after();
-        um::tmem_dealloc(tmem_base, 512);
+        um::tmem_dealloc2(tmem_base, 512);
     }
 }
 
@@ -552,48 +551,44 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
-// Clusters of kCluster CTAs share every B tile through TMA multicast.
-constexpr int kCluster = 2;
-
 template <int MODE>
-static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
-                       const CUtensorMap &b1, const UmmaArgs &args, cudaStream_t s)
+static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
+                       const UmmaArgs &args, cudaStream_t s)
 {
-    constexpr int C = kCluster;
-    auto kern = k_umma<MODE, C>;
+    auto kern = k_umma<MODE>;
+    constexpr int smem = Cfg<MODE>::kSmem;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const long long groups = (args.n_mtiles + C - 1) / C;
-    const long long items = (long long)args.LB * groups * (MODE == M_DIST ? args.max_chunks : args.n_ntiles);
+    const long long items = (long long)args.LB * args.tiles_t * args.tiles_n;
     if (items <= 0) return cudaSuccess;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-        cfg.gridDim = dim3(C * 64, 1, 1);
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, (void *)kern, &cfg);
-        if (e != cudaSuccess || max_clusters <= 0) max_clusters = device_sm_count() / C;
+    static int max_pairs = 0;
+    if (max_pairs == 0) {
+        cfg.gridDim = dim3(2 * 64, 1, 1);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)kern, &cfg);
+        if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
     }
-    const long long nc = items < max_clusters ? items : max_clusters;
-    cfg.gridDim = dim3((unsigned)(nc * C), 1, 1);
+    const long long np = items < max_pairs ? items : max_pairs;
+    cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
     static const char *names[4] = {"umma_ref_proj", "umma_distance_topk", "umma_swiglu_diff",
                                    "umma_z_quant"};
     ProfScope prof(names[MODE], s);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a0, a1, b, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -617,7 +612,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
 
     UmmaArgs a{};
     a.LB = g.LB; a.B = g.B; a.T = g.T; a.W = g.W; a.d_ff = g.d_ff; a.d_c = g.d_c;
-    a.n_ref = g.n_ref; a.bits = g.bits; a.max_chunks = g.max_chunks;
+    a.n_ref = g.n_ref; a.bits = g.bits;
     a.P1 = P1; a.P2 = P2; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
     a.ref_slot = pool->ref_slot; a.cand = cand; a.ref_idx = (const int4 *)cache->ref_idx;
     uint8_t *copy_flag = ws + wl.copy_flag;
@@ -625,33 +620,30 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     a.dh_hi = dh_hi; a.dh_lo = dh_lo; a.codes = cache->codes; a.hdr = (float2 *)cache->hdr;
     a.z_out = z_out; a.status = status;
     const int kw = (g.W + kBK - 1) / kBK;
+    const int ff_slices = (g.d_ff + kBM - 1) / kBM;
 
-    CUtensorMap mX, mW1, mW2, mW3, mHi, mLo, mRa, mRb;
-    // B maps load one cluster slice per box: kBN / kCluster rows
-    constexpr int kSliceRows = kBN / kCluster;
-    static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster of 1, 2 or 4");
-    const int split_rows = kCluster == 1 ? kBN / 2 : kSliceRows;
-    if (!make_map(&mX, kv, g.W, g.T, g.LB, kBM) || !make_map(&mW1, W1t, g.W, g.d_ff, g.L, split_rows) ||
-        !make_map(&mW2, W2t, g.W, g.d_ff, g.L, split_rows) ||
-        !make_map(&mW3, W3t, g.d_ff, g.d_c, g.L, kSliceRows) ||
+    // token and reference rows: 128 per CTA; W_c1 / W_c2: 64 rows each per CTA;
+    // W_c3: 128 rows (one CTA's half of a 256-column d_c tile)
+    CUtensorMap mX, mW1, mW2, mW3, mHi, mLo, mR;
+    if (!make_map(&mX, kv, g.W, g.T, g.LB, kBM) || !make_map(&mW1, W1t, g.W, g.d_ff, g.L, kBM / 2) ||
+        !make_map(&mW2, W2t, g.W, g.d_ff, g.L, kBM / 2) ||
+        !make_map(&mW3, W3t, g.d_ff, g.d_c, g.L, kHalfN) ||
         !make_map(&mHi, dh_hi, g.d_ff, g.T, g.LB, kBM) ||
         !make_map(&mLo, dh_lo, g.d_ff, g.T, g.LB, kBM))
         return cudaErrorInvalidValue;
 
     if (g.n_ref > 0) {
-        if (!make_map(&mRa, ref_mma, g.W, g.n_ref, g.LB, kBM) ||
-            !make_map(&mRb, ref_mma, g.W, g.n_ref, g.LB, kSliceRows))
-            return cudaErrorInvalidValue;
+        if (!make_map(&mR, ref_mma, g.W, g.n_ref, g.LB, kHalfN)) return cudaErrorInvalidValue;
         // P1 | P2 for every reference
         UmmaArgs p = a;
-        p.rows = g.n_ref; p.n_mtiles = (g.n_ref + kBM - 1) / kBM; p.n_ntiles = (g.d_ff + 127) / 128;
-        p.k_chunks = kw; p.a_sources = 1; p.b_split = 1; p.b_per_layer = 1;
-        if ((e = run<M_P>(mRa, mRa, mW1, mW2, p, s)) != cudaSuccess) return e;
+        p.rows = g.n_ref; p.tiles_t = (g.n_ref + kTileM - 1) / kTileM; p.tiles_n = ff_slices;
+        p.k_chunks = kw; p.a_sources = 1;
+        if ((e = run<M_P>(mW1, mW2, mR, p, s)) != cudaSuccess) return e;
         // distance expansion and per-item candidates
         UmmaArgs d = a;
-        d.rows = g.T; d.n_mtiles = g.n_mtiles; d.n_ntiles = 1;
-        d.k_chunks = kw; d.a_sources = 1; d.b_split = 0; d.b_per_layer = 0;
-        if ((e = run<M_DIST>(mX, mX, mRb, mRb, d, s)) != cudaSuccess) return e;
+        d.rows = g.T; d.tiles_t = g.n_mtiles; d.tiles_n = g.max_chunks;
+        d.k_chunks = kw; d.a_sources = 1;
+        if ((e = run<M_DIST>(mX, mX, mR, d, s)) != cudaSuccess) return e;
     }
     int32_t *scan_list = (int32_t *)(ws + wl.scan_list);
     float *xnorm = (float *)(ws + wl.xnorm);
@@ -662,15 +654,15 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         return e;
     {
         UmmaArgs p = a;
-        p.rows = g.T; p.n_mtiles = g.n_mtiles; p.n_ntiles = (g.d_ff + 127) / 128;
-        p.k_chunks = kw; p.a_sources = 1; p.b_split = 1; p.b_per_layer = 1;
-        if ((e = run<M_S1>(mX, mX, mW1, mW2, p, s)) != cudaSuccess) return e;
+        p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = ff_slices;
+        p.k_chunks = kw; p.a_sources = 1;
+        if ((e = run<M_S1>(mW1, mW2, mX, p, s)) != cudaSuccess) return e;
     }
     {
         UmmaArgs p = a;
-        p.rows = g.T; p.n_mtiles = g.n_mtiles; p.n_ntiles = (g.d_c + kBN - 1) / kBN;
-        p.k_chunks = (g.d_ff + kBK - 1) / kBK; p.a_sources = 2; p.b_split = 0; p.b_per_layer = 1;
-        if ((e = run<M_S2>(mHi, mLo, mW3, mW3, p, s)) != cudaSuccess) return e;
+        p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = (g.d_c + kBN - 1) / kBN;
+        p.k_chunks = (g.d_ff + kBK - 1) / kBK; p.a_sources = 2;
+        if ((e = run<M_S2>(mHi, mLo, mW3, p, s)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
