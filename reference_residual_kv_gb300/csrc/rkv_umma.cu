@@ -482,13 +482,14 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 }
-                // this warp is done with the accumulator: one arrival on the leader's
-                // barrier (which counts both CTAs' epilogue warps)
+                // this warp is done with the accumulator (every tcgen05.ld has been
+                // waited for): one relaxed arrival on the leader's barrier, which counts
+                // both CTAs' epilogue warps; the warp's stores need no ordering with it
                 um::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (leader) um::mbar_arrive(&tempty[buf]);
-                    else um::mbar_arrive_cluster(um::mapa(um::smem_u32(&tempty[buf]), 0));
+                    if (leader) um::mbar_arrive_relaxed(&tempty[buf]);
+                    else um::mbar_arrive_cluster_relaxed(um::mapa(um::smem_u32(&tempty[buf]), 0));
                 }
                 ++cnt;
             }
