@@ -224,7 +224,9 @@ def read_path(dev, steps=256, reps=3):
     cfg = wl.CONFIGS["long-131k-fp8ref"]
     kv = torch.from_numpy(wl.layer_kv(cfg, 0)[None].view(np.int16)).view(torch.bfloat16).to(dev)
     w = wl.layer_weights(cfg, 0)
-    W1, W2, W3 = (torch.from_numpy(x[None].view(np.int16)).view(torch.bfloat16).to(dev) for x in w)
+    G = torch.from_numpy(np.stack([w[0][None], w[1][None]]).view(np.int16)).view(torch.bfloat16).to(dev)
+    W1, W2 = G[0], G[1]
+    W3 = torch.from_numpy(w[2][None].view(np.int16)).view(torch.bfloat16).to(dev)
     p = rkv.params_from_config(cfg)
     bufs = rkv.Buffers(p, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -300,11 +302,14 @@ def run_ours(args, cfg):
 
     kv, w = _gen_inputs(cfg)
     kv_h = torch.from_numpy(np.stack(kv).view(np.int16)).view(torch.bfloat16).pin_memory()
-    W1_h = torch.from_numpy(np.stack([x[0] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    W2_h = torch.from_numpy(np.stack([x[1] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    # W_c1 and W_c2 of all layers in one allocation [2][L][d_ff][W] (the library loads a
+    # stage's two gate halves as one tile when W_c2 follows W_c1)
+    G_h = torch.from_numpy(np.stack([np.stack([x[0] for x in w]), np.stack([x[1] for x in w])])
+                           .view(np.int16)).view(torch.bfloat16).pin_memory()
     W3_h = torch.from_numpy(np.stack([x[2] for x in w]).view(np.int16)).view(torch.bfloat16).pin_memory()
     del kv, w
-    kv_d, W1, W2, W3 = (t.to(dev) for t in (kv_h, W1_h, W2_h, W3_h))
+    kv_d, G, W3 = (t.to(dev) for t in (kv_h, G_h, W3_h))
+    W1, W2 = G[0], G[1]
 
     p = rkv.params_from_config(cfg)
     bufs = rkv.Buffers(p, device=dev)
@@ -363,12 +368,12 @@ def run_ours(args, cfg):
     if not args.no_e2e:
         res_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                  for t in (bufs.codes, bufs.hdr, bufs.ref_idx, bufs.ref_vec, bufs.ref_sqnorm, out_z, out_m)]
-        h2d = sum(t.numel() * t.element_size() for t in (kv_h, W1_h, W2_h, W3_h))
+        h2d = sum(t.numel() * t.element_size() for t in (kv_h, G_h, W3_h))
         d2h = sum(t.numel() * t.element_size() for t in res_h)
         srcs = (bufs.codes, bufs.hdr, bufs.ref_idx, bufs.ref_vec, bufs.ref_sqnorm, out_z, out_m)
 
         def e2e_step():
-            for d, h in zip((kv_d, W1, W2, W3), (kv_h, W1_h, W2_h, W3_h)):
+            for d, h in zip((kv_d, G, W3), (kv_h, G_h, W3_h)):
                 d.copy_(h, non_blocking=True)
             step()
             for h, d in zip(res_h, srcs):
@@ -438,7 +443,7 @@ def run_ours(args, cfg):
         "e2e": e2e,
     }
     if not args.no_read_path:
-        del kv_d, W1, W2, W3, bufs, out_z, out_m
+        del kv_d, G, W1, W2, W3, bufs, out_z, out_m
         torch.cuda.empty_cache()
         line["read_path"] = read_path(dev)
     if not args.no_cpu_baseline and ws >= 1:

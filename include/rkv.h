@@ -132,6 +132,9 @@ rkv_status rkv_build_ref_pool(const rkv_params *p, const void *kv, const rkv_ref
  *     `bits` bits (a constant group is stored exactly: delta = 0).
  * Weights are stored out-major, one set per layer, in kv_dtype:
  *  W1t, W2t: [L][d_ff][W] with W1t[f][c] = W_c1[c][f];  W3t: [L][d_c][d_ff].
+ *  (bf16 path: if W2t lies at a positive multiple of 16 bytes after W1t, e.g. both in
+ *  one allocation, the two gate halves load as one tile per pipeline stage, which is
+ *  faster; any other placement is equally correct.)
  * workspace: >= workspace_bytes from rkv_query_sizes, 256-byte aligned.
  * z_out (nullable): [L*B][T][d_c] fp32 unquantised z (0 for reference tokens).
  * dev_status: device int32, set to RKV_OK by the caller.                         */

@@ -17,7 +17,8 @@
 // writes directly (the tensor cores need not round the token's and the
 // references' projections identically, since they sit in different tile rows).
 // Exact distances sum (x - r)^2 in fp32: for bf16 data x - r is exact, each group of
-// 8 squares is added as a tree, and the warp adds its lanes as a tree.
+// 8 squares is added as a tree, a lane keeps four partial sums over its groups, and the
+// warp adds its lanes as a tree.
 // Without candidates (the fp32 path) every token takes the full scan, one warp per
 // token.  On the tensor-core path the (rare) full scans are deferred to
 // k_topk_fullscan: the token is appended to a list and a whole block scans its pool,
@@ -54,23 +55,36 @@ __device__ __forceinline__ float warp_tree_sum(float v)
 }
 
 template <typename T>
+__device__ __forceinline__ float sq8(const T *x, const T *r)
+{
+    float a[8], b[8], s[8];
+    Vec8<T>::load(x, a);
+    Vec8<T>::load(r, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float d = a[j] - b[j];
+        s[j] = d * d;
+    }
+    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
+// Exact squared distance of two rows, summed by the whole warp: each lane's 8-element
+// groups are squared and added as trees, four groups of the lane in flight at once
+// (independent partial sums), and the lanes are added as a tree.
+template <typename T>
 __device__ __forceinline__ float warp_sqdist(const T *x, const T *r, int W, int lane)
 {
-    float acc = 0.0f;
-    for (int c = lane * 8; c < W; c += 256) {
-        float a[8], b[8];
-        Vec8<T>::load(x + c, a);
-        Vec8<T>::load(r + c, b);
-        float s[8];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int c = lane * 8;
+    for (; c + 3 * 256 < W; c += 4 * 256) {
+        float p[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float d = a[j] - b[j];
-            s[j] = d * d;
-        }
-        float s8 = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-        acc += s8;
+        for (int u = 0; u < 4; ++u) p[u] = sq8(x + c + u * 256, r + c + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] += p[u];
     }
-    return warp_tree_sum(acc);
+    for (; c < W; c += 256) acc[0] += sq8(x + c, r + c);
+    return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
 
 template <typename T>
@@ -216,17 +230,24 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
 #pragma unroll
             for (int j = 0; j <= kMaxK; ++j) { te[j] = INFINITY; ts[j] = kNoSlot; }
             float e_last = INFINITY;   // smallest last entry of a full list
-            for (int li = 0; li < nlists; ++li) {
-                const float4 *lp = cp + li * (kList / 2);
-                const float4 tail = lp[kList / 2 - 1];
-                if (__float_as_int(tail.w) >= 0) e_last = fminf(e_last, tail.z);
-                for (int j = 0; j < kList / 2; ++j) {
-                    const float4 c = j == kList / 2 - 1 ? tail : lp[j];
-                    const int s0 = __float_as_int(c.y), s1 = __float_as_int(c.w);
-                    if (s0 < 0 || !key_less(c.x, s0, te[kMaxK], ts[kMaxK])) break;
-                    list_insert<kMaxK + 1>(te, ts, c.x, s0);
-                    if (s1 < 0 || !key_less(c.z, s1, te[kMaxK], ts[kMaxK])) break;
-                    list_insert<kMaxK + 1>(te, ts, c.z, s1);
+            for (int ch = 0; ch < nch; ++ch) {
+                // the work item's two sorted lists, all 8 float4 loads in flight at once
+                float4 e4[kCand / 2];
+#pragma unroll
+                for (int j = 0; j < kCand / 2; ++j) e4[j] = cp[ch * (kCand / 2) + j];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 tail = e4[h * (kList / 2) + kList / 2 - 1];
+                    if (__float_as_int(tail.w) >= 0) e_last = fminf(e_last, tail.z);
+#pragma unroll
+                    for (int j = 0; j < kList / 2; ++j) {
+                        const float4 c = e4[h * (kList / 2) + j];
+                        const int s0 = __float_as_int(c.y), s1 = __float_as_int(c.w);
+                        if (s0 < 0 || !key_less(c.x, s0, te[kMaxK], ts[kMaxK])) break;
+                        list_insert<kMaxK + 1>(te, ts, c.x, s0);
+                        if (s1 < 0 || !key_less(c.z, s1, te[kMaxK], ts[kMaxK])) break;
+                        list_insert<kMaxK + 1>(te, ts, c.z, s1);
+                    }
                 }
             }
             const float xn = xnorm[gt];

@@ -63,6 +63,7 @@ struct UmmaArgs {
     int tiles_n;          // M_P/M_S1: 128-column d_ff slices; M_S2: 256-column d_c tiles;
                           // M_DIST: distance chunks (max_chunks)
     int k_chunks, a_sources;
+    int fused_gate;       // M_P/M_S1: tmA0 maps W_c1 and W_c2 together (one box per stage)
     int W, d_ff, d_c, n_ref, bits;
     float *P1, *P2;
     const float *ref_sqnorm;
@@ -107,6 +108,15 @@ __device__ __forceinline__ bool item_get(const UmmaArgs &a, int i, Item &it)
     it.n0 = n;
     it.n1 = n + 1;
     return true;
+}
+
+// M_DIST: MMA N of N-tile n of pair tile t: the references the tile's last row can see,
+// rounded up to 32 (so that each CTA's half is a multiple of 16 rows); CTA r of the pair
+// supplies references [n*256 + r*N/2, n*256 + (r+1)*N/2).
+__device__ __forceinline__ int dist_cols(const UmmaArgs &a, int t, int n)
+{
+    const int own = a.pool_size[min(a.T, (t + 1) * kTileM) - 1] - n * kBN;
+    return own >= kBN ? kBN : ((own + 31) & ~31);
 }
 
 // Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
@@ -196,14 +206,19 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             // A: 64 rows of W_c1 and the same 64 rows of W_c2; B: 128 tokens
                             const int f0 = n * kBM + (int)rank * (kBM / 2);
                             const int lz = it.lb / a.B;
-                            um::tma_load_3d_pair(sa, &tmA0, bar, kx, f0, lz);
-                            um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, f0, lz);
+                            if (a.fused_gate) {
+                                um::tma_load_4d_pair(sa, &tmA0, bar, kx, f0, lz, 0);
+                            } else {
+                                um::tma_load_3d_pair(sa, &tmA0, bar, kx, f0, lz);
+                                um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, f0, lz);
+                            }
                             um::tma_load_3d_pair(sb, &tmB, bar, kx, it.t * 2 * kBM + (int)rank * kBM, it.lb);
                         } else {
                             // A: 128 token rows (M_S2: dh_hi, then dh_lo); B: half of N tile n
                             um::tma_load_3d_pair(sa, src ? &tmA1 : &tmA0, bar, kx,
                                                  it.t * 2 * kBM + (int)rank * kBM, it.lb);
-                            um::tma_load_3d_pair(sb, &tmB, bar, kx, n * kBN + (int)rank * kHalfN,
+                            const int half = MODE == M_DIST ? dist_cols(a, it.t, n) / 2 : kHalfN;
+                            um::tma_load_3d_pair(sb, &tmB, bar, kx, n * kBN + (int)rank * half,
                                                  MODE == M_S2 ? it.lb / a.B : it.lb);
                         }
                         used[stage] = true;
@@ -238,6 +253,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     um::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
+                    // distance tiles: only the references the tile's rows can see
+                    const uint32_t id = MODE == M_DIST ? um::idesc_bf16_f32(2 * kBM, dist_cols(a, it.t, n)) : kIdesc;
                     for (int kc = 0; kc < k_iters; ++kc) {
                         const bool wf = um::mbar_wait(&full[stage], ph, kWaitCycles);
                         if (*abort_flag || !wf) {
@@ -250,7 +267,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const uint64_t bd = um::sdesc_sw128(sa + kABytes);
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
-                            um::mma2_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (kc | k) != 0);
+                            um::mma2_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id, (kc | k) != 0);
                         um::mma2_commit_mc(&empty[stage], kPairMask);
                         if (++stage == S) { stage = 0; ph ^= 1u; }
                     }
@@ -552,6 +569,24 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// W_c1 and W_c2 ([L][d_ff][W] each) seen as one [2][L][d_ff][W] tensor whose matrix
+// stride is the distance between them: box = 64 (inner) x 64 rows x 1 layer x both
+// matrices, i.e. 64 rows of W_c1 followed by the same 64 rows of W_c2.
+static bool make_map_gates(CUtensorMap *m, const void *W1, long long gate_off, uint64_t inner,
+                           uint64_t rows, uint64_t layers)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {inner, rows, layers, 2};
+    cuuint64_t strides[3] = {inner * 2, inner * 2 * rows, (cuuint64_t)gate_off};
+    cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)(kBM / 2), 1, 2};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(W1), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int MODE>
 static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                        const UmmaArgs &args, cudaStream_t s)
@@ -622,6 +657,10 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     a.z_out = z_out; a.status = status;
     const int kw = (g.W + kBK - 1) / kBK;
     const int ff_slices = (g.d_ff + kBM - 1) / kBM;
+    // W_c2 at a 16-byte multiple after W_c1 (e.g. both in one allocation): the two gate
+    // halves of a stage come in one TMA box
+    const long long gate_off = (long long)((const char *)W2t - (const char *)W1t);
+    const bool fused = gate_off > 0 && gate_off % 16 == 0 && gate_off < (1ll << 40);
 
     // token and reference rows: 128 per CTA; W_c1 / W_c2: 64 rows each per CTA;
     // W_c3: 128 rows (one CTA's half of a 256-column d_c tile)
@@ -633,13 +672,18 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         !make_map(&mLo, dh_lo, g.d_ff, g.T, g.LB, kBM))
         return cudaErrorInvalidValue;
 
+    CUtensorMap mG1 = mW1;
+    if (fused) {
+        if (!make_map_gates(&mG1, W1t, gate_off, g.W, g.d_ff, g.L)) return cudaErrorInvalidValue;
+        a.fused_gate = 1;
+    }
     if (g.n_ref > 0) {
         if (!make_map(&mR, ref_mma, g.W, g.n_ref, g.LB, kHalfN)) return cudaErrorInvalidValue;
         // P1 | P2 for every reference
         UmmaArgs p = a;
         p.rows = g.n_ref; p.tiles_t = (g.n_ref + kTileM - 1) / kTileM; p.tiles_n = ff_slices;
         p.k_chunks = kw; p.a_sources = 1;
-        if ((e = run<M_P>(mW1, mW2, mR, p, s)) != cudaSuccess) return e;
+        if ((e = run<M_P>(mG1, mW2, mR, p, s)) != cudaSuccess) return e;
         // distance expansion and per-item candidates
         UmmaArgs d = a;
         d.rows = g.T; d.tiles_t = g.n_mtiles; d.tiles_n = g.max_chunks;
@@ -657,7 +701,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         UmmaArgs p = a;
         p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = ff_slices;
         p.k_chunks = kw; p.a_sources = 1;
-        if ((e = run<M_S1>(mW1, mW2, mX, p, s)) != cudaSuccess) return e;
+        if ((e = run<M_S1>(mG1, mW2, mX, p, s)) != cudaSuccess) return e;
     }
     {
         UmmaArgs p = a;

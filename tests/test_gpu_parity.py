@@ -77,6 +77,29 @@ def test_full_size_sampled(name, layers):
     _parity(cfg, n_sample=n, layers_checked=layers, all_idx=False)
 
 
+def test_gate_weight_placement_gives_identical_records():
+    # W_c2 after W_c1 at a 16-byte multiple is loaded with one TMA box per stage, the
+    # other order with two; both must give bit-identical records
+    cfg = SMALL["llama-2x1000"]
+    kv, w = gen_inputs(cfg)
+    kv_d = to_device(np.stack(kv), cfg.kv_dtype)
+    W1 = np.stack([x[0] for x in w])
+    W2 = np.stack([x[1] for x in w])
+    W3 = to_device(np.stack([x[2] for x in w]), cfg.kv_dtype)
+    after = to_device(np.stack([W1, W2]), cfg.kv_dtype)       # [W_c1 | W_c2]
+    before = to_device(np.stack([W2, W1]), cfg.kv_dtype)      # [W_c2 | W_c1]
+    recs = []
+    for w1, w2 in ((after[0], after[1]), (before[1], before[0])):
+        bufs = rkv.Buffers(rkv.params_from_config(cfg), want_z=True)
+        bufs.build_ref_pool(kv_d)
+        bufs.compress(kv_d, w1, w2, W3)
+        torch.cuda.synchronize()
+        assert bufs.device_status() == 0
+        recs.append(host_records(cfg, bufs))
+    for key in ("idx", "q", "hdr", "z"):
+        assert np.array_equal(recs[0][key], recs[1][key]), key
+
+
 def test_edge_cases_small_T_first_offset_k():
     base = C["llama3.1-8b-kv"].replace(L=1, N=2, D=64, d_ff=256, d_c=64)
     for cfg in (base.replace(T=1), base.replace(T=9), base.replace(T=130),
