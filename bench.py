@@ -35,6 +35,14 @@ METRIC = "tokens compressed/sec (Llama-3.1-8B KV shape) and % of bf16 tensor roo
 UNIT = "tokens/s"
 
 
+# DRAM bytes (read + write) per launch of a kernel on this workload, from one ncu capture
+# of a 4-layer case scaled to 32 layers by the units processed (its traffic grows in
+# proportion): profiles/k_umma_swiglu_diff_and_distance_llama3.1-8b-kv_4layers.md.
+# Set an entry to None when its kernel changes.
+NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (200.954368e6 + 108.118528e6),
+                  "umma_distance_topk": 8 * (165.357312e6 + 4.224256e6)}
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -426,7 +434,8 @@ def run_ours(args, cfg):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
         "config": workload_description(cfg),
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tf_sust,
-                     "unit": "TFLOP/s", "frac": achieved / tf_sust, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / tf_sust,
+                     "traffic": NCU_DRAM_BYTES.get(dom) if cfg.L == 32 else None,
                      "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % src,
                      "algorithmic_flops_per_launch": fl[dom]},
         "compress_roofline": {"flops_per_step": f_alg, "ms_per_step": compress_ms,
