@@ -35,10 +35,10 @@ METRIC = "tokens compressed/sec (Llama-3.1-8B KV shape) and % of bf16 tensor roo
 UNIT = "tokens/s"
 
 
-# DRAM bytes (read + write) per launch of a kernel on this workload, from one ncu capture
-# of a 4-layer case scaled to 32 layers by the units processed (its traffic grows in
-# proportion): profiles/k_umma_swiglu_diff_and_distance_llama3.1-8b-kv_4layers.md.
-# Set an entry to None when its kernel changes.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a kernel on
+# this workload, from one `ncu --set full` capture of the 4-layer case scaled to 32
+# layers by the units processed (its traffic grows in proportion).  Set an entry to None
+# when its kernel changes.
 NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (200.954368e6 + 108.118528e6),
                   "umma_distance_topk": 8 * (165.357312e6 + 4.224256e6)}
 
