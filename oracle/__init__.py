@@ -288,3 +288,38 @@ def retrieve_tokens(cfg: wl.Config, kv_seq, tokens, kv64=None, refs64=None, ref_
     lib().rkvo_retrieve_tokens(cfg.W, cfg.k, pkv, prf, ppos, ref_pos.size, ptok, n,
                                idx.ctypes.data_as(_ip), ki.ctypes.data_as(_ip), dk.ctypes.data_as(_dp))
     return idx, ki, dk
+
+
+def rope(x, pos: float, base: float) -> np.ndarray:
+    """Rotary embedding of one head vector x [D] at position pos (consecutive pairs)."""
+    x = np.array(x, dtype=np.float64)
+    lib().rkvo_rope(x.ctypes.data_as(_dp), x.size, ctypes.c_double(pos), ctypes.c_double(base))
+    return x
+
+
+def decode(z, Wd) -> np.ndarray:
+    """Linear decoder f_d(z) = z W_d with Wd stored out-major [W][d_c]."""
+    z, pz = _d(z)
+    Wd, pw = _d(Wd)
+    out = np.zeros(Wd.shape[0])
+    lib().rkvo_decode(pz, pw, z.size, Wd.shape[0], out.ctypes.data_as(_dp))
+    return out
+
+
+def restore(cfg: wl.Config, refs64, q, zmin, delta, idx, Wd64, sel):
+    """Restored K^, V^ [n_sel][N*D] of the selected tokens of one sequence (K^ rotated at
+    each token's position), from records [T][...] and the decoder weights [W][d_c]."""
+    refs64, prf = _d(refs64)
+    q, pq = _u(q)
+    zmin, pmn = _d(zmin)
+    delta, pdl = _d(delta)
+    idx, pidx = _i(idx)
+    Wd64, pw = _d(Wd64)
+    sel, psel = _i(sel)
+    n = sel.size
+    ko = np.zeros((n, cfg.N * cfg.D))
+    vo = np.zeros((n, cfg.N * cfg.D))
+    lib().rkvo_restore(cfg.N, cfg.D, cfg.d_c, cfg.group, cfg.k, ctypes.c_double(cfg.rope_base),
+                       prf, pq, pmn, pdl, pidx, pw, psel, n, ko.ctypes.data_as(_dp),
+                       vo.ctypes.data_as(_dp))
+    return ko, vo

@@ -371,3 +371,63 @@ void rkvo_retrieve_tokens(int W, int k, const double *kv, const double *refs,
         ki_out[n] = rkvo_retrieve(kv + (size_t)t * W, refs, n_pool, W, k, ix, dk + 2 * n);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Rotary position embedding of one head of dimension D at position pos.  §2.1
+ * (implementation requirement) says the restored pre-RoPE key must be rotated at the
+ * token's own position before RoPE attention; the page does not fix the RoPE variant.
+ * Reading: the rotary embedding as first defined (RoFormer): consecutive coordinate
+ * pairs (x_{2i}, x_{2i+1}), i = 0 .. D/2-1, rotated by the angle pos * theta_i with
+ * theta_i = base^(-2i/D):
+ *   x'_{2i}   = x_{2i} cos(a) - x_{2i+1} sin(a)
+ *   x'_{2i+1} = x_{2i} sin(a) + x_{2i+1} cos(a).                                   */
+void rkvo_rope(double *x, int D, double pos, double base)
+{
+    for (int i = 0; i < D / 2; i++) {
+        double theta = pow(base, -2.0 * (double)i / (double)D);
+        double a = pos * theta;
+        double c = cos(a), s = sin(a);
+        double x0 = x[2 * i], x1 = x[2 * i + 1];
+        x[2 * i] = x0 * c - x1 * s;
+        x[2 * i + 1] = x0 * s + x1 * c;
+    }
+}
+
+/* §2.5 = Sec. IV-B, linear decoder without bias: f_d(z) = z W_d, W_d in R^{d_c x 2d_k},
+ * stored out-major: Wd[c][j] = W_d[j][c], c < 2 d_k.                               */
+void rkvo_decode(const double *z, const double *Wd, int d_c, int W, double *out)
+{
+    for (int c = 0; c < W; c++) {
+        double s = 0.0;
+        for (int j = 0; j < d_c; j++) s += z[j] * Wd[(size_t)c * d_c + j];
+        out[c] = s;
+    }
+}
+
+/* §2.5 = Sec. IV-B and §2.7 = Sec. IV-C, restoring the selected tokens of one sequence:
+ *   KV^_t = f_d(z~_t) + mean_t,   then split: K^ = KV^[0, N D), V^ = KV^[N D, 2 N D),
+ *   heads in order (head h = coordinates [h D, (h+1) D) of each half);
+ * the key of every head is rotated at the token's own position t (rkvo_rope);
+ * z~_t and mean_t are the sparse read of rkvo_gather.  Outputs [n_sel][N D] each.     */
+void rkvo_restore(int N, int D, int d_c, int group, int k, double rope_base,
+                  const double *refs, const uint8_t *q, const double *zmin, const double *delta,
+                  const int32_t *idx, const double *Wd, const int32_t *sel, int n_sel,
+                  double *k_out, double *v_out)
+{
+    int dk = N * D, W = 2 * dk;
+    double *zq = malloc(sizeof(double) * d_c);
+    double *mean = malloc(sizeof(double) * W);
+    double *dec = malloc(sizeof(double) * W);
+    for (int n = 0; n < n_sel; n++) {
+        int32_t one = sel[n];
+        rkvo_gather(W, d_c, group, k, refs, q, zmin, delta, idx, &one, 1, zq, mean);
+        rkvo_decode(zq, Wd, d_c, W, dec);
+        double *ko = k_out + (size_t)n * dk, *vo = v_out + (size_t)n * dk;
+        for (int c = 0; c < dk; c++) {
+            ko[c] = dec[c] + mean[c];
+            vo[c] = dec[dk + c] + mean[dk + c];
+        }
+        for (int h = 0; h < N; h++) rkvo_rope(ko + (size_t)h * D, D, (double)one, rope_base);
+    }
+    free(zq); free(mean); free(dec);
+}

@@ -29,6 +29,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # stream tags (purpose of a random stream)
 TAG_CENT, TAG_CID, TAG_NOISE, TAG_COPYFLAG, TAG_COPYSRC = 1, 2, 3, 4, 5
 TAG_PATCH, TAG_W1, TAG_W2, TAG_W3, TAG_SEL, TAG_USER = 6, 7, 8, 9, 10, 11
+TAG_WD, TAG_REC, TAG_QUERY = 12, 13, 14
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -139,6 +140,7 @@ class Config:
     gather_frac: float = 0.3
     gather_tail: int = 512
     gather_steps: int = 0
+    rope_base: float = 10000.0  # base of the rotary embedding applied to restored keys
 
     @property
     def W(self) -> int:
@@ -266,6 +268,41 @@ def layer_weights(cfg: Config, layer: int):
     w2 = normal(stream_key(s, TAG_W2, layer), F * W).reshape(F, W) * math.sqrt(1.0 / W)
     w3 = normal(stream_key(s, TAG_W3, layer), C * F).reshape(C, F) * math.sqrt(1.0 / F)
     return store(w1, cfg.kv_dtype), store(w2, cfg.kv_dtype), store(w3, cfg.kv_dtype)
+
+
+def decoder_weights(cfg: Config, layer: int):
+    """Stored linear-decoder weights of one layer, out-major: Wd [W][d_c]
+    (Wd[c][j] = W_d[j][c]), entries ~ N(0, 1/d_c)."""
+    w = normal(stream_key(cfg.seed, TAG_WD, layer), cfg.W * cfg.d_c).reshape(cfg.W, cfg.d_c)
+    return store(w * math.sqrt(1.0 / cfg.d_c), cfg.kv_dtype)
+
+
+def synthetic_records(cfg: Config, n_ref: int, lb: int = 0):
+    """Arbitrary well-formed cache records of one (layer, sequence), for testing the read
+    side on its own: codes [T][d_c] uniform in [0, 2^bits), group minima ~ N(0, 0.1^2),
+    steps ~ U(0, 0.05) with every 7th group constant (step 0), reference relations of
+    1..k distinct slots in [0, n_ref), ascending, -1 padded; and n_ref pool vectors
+    ~ N(0, 1) stored in ref_dtype (FP8: uniform non-NaN bytes).
+    Returns (codes, zmin, delta, ref_idx, refs)."""
+    T, C, G, k = cfg.T, cfg.d_c, cfg.d_c // cfg.group, cfg.k
+    key = lambda part: stream_key(cfg.seed, TAG_REC, lb, part)
+    codes = np.minimum(np.floor(uniform(key(0), T * C) * (1 << cfg.bits)),
+                       (1 << cfg.bits) - 1).astype(np.uint8).reshape(T, C)
+    zmin = (normal(key(1), T * G) * 0.1).reshape(T, G)
+    delta = (uniform(key(2), T * G) * 0.05).reshape(T, G)
+    delta[:, ::7] = 0.0
+    cnt = 1 + np.minimum(np.floor(uniform(key(3), T) * k), k - 1).astype(np.int64)
+    order = np.argsort(uniform(key(4), T * n_ref).reshape(T, n_ref), axis=1, kind="stable")
+    ref_idx = np.full((T, k), -1, np.int32)
+    for t in range(T):
+        ref_idx[t, :cnt[t]] = np.sort(order[t, :cnt[t]])
+    if cfg.ref_dtype == "fp8":
+        # stored FP8 bytes drawn directly: any byte but the two NaN codes 0x7f, 0xff
+        b = np.floor(uniform(key(5), n_ref * cfg.W) * 254).astype(np.int64)
+        refs = (b + (b >= 0x7f)).astype(np.uint8).reshape(n_ref, cfg.W)
+    else:
+        refs = store(normal(key(5), n_ref * cfg.W).reshape(n_ref, cfg.W), cfg.ref_dtype)
+    return codes, zmin.astype(np.float32), delta.astype(np.float32), ref_idx, refs
 
 
 def gather_selection(cfg: Config, step: int, seq: int = 0) -> np.ndarray:

@@ -26,6 +26,16 @@ MUTANTS = {
                                      "p = p + s0 + (long long)ceil(alpha * (double)(p - n_sink));"),
     "dequantise without the minimum": ("zq[c] = (double)q[c] * delta[c / group] + zmin[c / group];",
                                        "zq[c] = (double)q[c] * delta[c / group];"),
+    "RoPE on the value half": ("for (int h = 0; h < N; h++) rkvo_rope(ko + (size_t)h * D, D, (double)one, rope_base);",
+                               "for (int h = 0; h < N; h++) rkvo_rope(vo + (size_t)h * D, D, (double)one, rope_base);"),
+    "RoPE pairs half a head apart": ("double x0 = x[2 * i], x1 = x[2 * i + 1];",
+                                     "double x0 = x[i], x1 = x[i + D / 2];"),
+    "RoPE frequency exponent -i/D": ("double theta = pow(base, -2.0 * (double)i / (double)D);",
+                                     "double theta = pow(base, -(double)i / (double)D);"),
+    "RoPE rotates the other way": ("x[2 * i] = x0 * c - x1 * s;", "x[2 * i] = x0 * c + x1 * s;"),
+    "decoder weights transposed": ("s += z[j] * Wd[(size_t)c * d_c + j];", "s += z[j] * Wd[(size_t)j * W + c];"),
+    "keys take the value half of the decoder": ("ko[c] = dec[c] + mean[c];", "ko[c] = dec[dk + c] + mean[c];"),
+    "value without the reference mean": ("vo[c] = dec[dk + c] + mean[dk + c];", "vo[c] = dec[dk + c];"),
 }
 
 

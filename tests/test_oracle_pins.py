@@ -348,3 +348,104 @@ def test_record_bytes_layout():
     # INT4, d_c = 512: 256 B codes + 16 groups x 8 B extremes + 4 x 4 B slots
     assert storage.record_bytes(512, 4) == 256 + 128 + 16
     assert storage.record_bytes(512, 2) == 128 + 128 + 16
+
+
+# ------------------------------------------------------------------ restore (f_d, RoPE)
+def test_rope_closed_forms_and_pair_layout():
+    D = 4
+    # position 0 is the identity
+    x = np.array([0.3, -1.2, 2.0, 0.7])
+    assert np.array_equal(oracle.rope(x, 0.0, 10000.0), x)
+    # pair 0 has theta = 1: (1, 0) at position p becomes (cos p, sin p)
+    for p in (1.0, 2.0, 7.0):
+        r = oracle.rope([1.0, 0.0, 0.0, 0.0], p, 10000.0)
+        assert np.allclose(r, [math.cos(p), math.sin(p), 0.0, 0.0], atol=1e-15)
+    # base 4, D = 4: pair 1 has theta = 4^(-1/2) = 1/2; (0, 1) -> (-sin, cos)
+    r = oracle.rope([0.0, 0.0, 0.0, 1.0], 3.0, 4.0)
+    assert np.allclose(r, [0.0, 0.0, -math.sin(1.5), math.cos(1.5)], atol=1e-15)
+    # the rotated pairs are consecutive coordinates: energy never leaves its pair
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal(128)
+    r = oracle.rope(v, 1234.0, 10000.0)
+    assert np.allclose(r[0::2] ** 2 + r[1::2] ** 2, v[0::2] ** 2 + v[1::2] ** 2, rtol=1e-12)
+
+
+def test_rope_relative_position_property():
+    # <R(m) q, R(n) k> = <R(m - n) q, k>: attention scores depend on m - n only
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    for m, n in ((5.0, 3.0), (1000.0, 17.0), (131071.0, 131000.0)):
+        lhs = float(oracle.rope(q, m, 10000.0) @ oracle.rope(k, n, 10000.0))
+        rhs = float(oracle.rope(q, m - n, 10000.0) @ k)
+        assert abs(lhs - rhs) <= 1e-9 * (np.abs(q).sum() * np.abs(k).sum()), (m, n, lhs, rhs)
+
+
+def test_decoder_unit_vectors_select_weight_columns():
+    rng = np.random.default_rng(7)
+    Wd = rng.standard_normal((12, 5))        # out-major [W][d_c]
+    for j in range(5):
+        e = np.zeros(5)
+        e[j] = 1.0
+        assert np.array_equal(oracle.decode(e, Wd), Wd[:, j])
+    assert np.array_equal(oracle.decode(np.zeros(5), Wd), np.zeros(12))
+    assert np.array_equal(oracle.decode([2.0, 0, 0, 0, -1.0], Wd), 2.0 * Wd[:, 0] - Wd[:, 4])
+
+
+def _restore_case(T=6, n_ref=3, seed=8):
+    cfg = wl.Config("restore-pin", seed=0, L=1, B=1, T=T, N=2, D=8, d_ff=8, d_c=64, k=4,
+                    group=32, bits=4, kv_dtype="f32", ref_dtype="f32", rope_base=10000.0)
+    rng = np.random.default_rng(seed)
+    refs = rng.standard_normal((n_ref, cfg.W))
+    Wd = rng.standard_normal((cfg.W, cfg.d_c)) * 0.1
+    q = rng.integers(0, 16, (T, cfg.d_c)).astype(np.uint8)
+    zmin = rng.standard_normal((T, 2)) * 0.1
+    delta = rng.uniform(0.0, 0.05, (T, 2))
+    idx = np.full((T, 4), -1, np.int32)
+    return cfg, refs, Wd, q, zmin, delta, idx
+
+
+def test_restore_reference_token_is_the_rotated_reference():
+    cfg, refs, Wd, q, zmin, delta, idx = _restore_case()
+    dk = cfg.N * cfg.D
+    # token 4 is a reference record: own slot, z = 0 (codes 0, extremes {0, 0})
+    idx[4, 0] = 2
+    q[4] = 0
+    zmin[4] = 0.0
+    delta[4] = 0.0
+    K, V = oracle.restore(cfg, refs, q, zmin, delta, idx, Wd, np.array([4], np.int32))
+    assert np.array_equal(V[0], refs[2, dk:])                   # the value half, unrotated
+    for h in range(cfg.N):                                       # each key head, rotated at 4
+        want = oracle.rope(refs[2, h * cfg.D:(h + 1) * cfg.D], 4.0, cfg.rope_base)
+        assert np.allclose(K[0, h * cfg.D:(h + 1) * cfg.D], want, rtol=0, atol=1e-14)
+
+
+def test_restore_moves_only_keys_with_position_and_is_affine_in_the_minima():
+    cfg, refs, Wd, q, zmin, delta, idx = _restore_case()
+    dk = cfg.N * cfg.D
+    # tokens 1 and 5 carry the same record: same V, keys rotated by the position gap
+    idx[1, :2] = [0, 2]
+    idx[5] = idx[1]
+    q[5], zmin[5], delta[5] = q[1], zmin[1], delta[1]
+    K, V = oracle.restore(cfg, refs, q, zmin, delta, idx, Wd, np.array([1, 5], np.int32))
+    assert np.array_equal(V[0], V[1])
+    for h in range(cfg.N):
+        k1 = K[0, h * cfg.D:(h + 1) * cfg.D]
+        assert np.allclose(oracle.rope(k1, 4.0, cfg.rope_base), K[1, h * cfg.D:(h + 1) * cfg.D],
+                           rtol=0, atol=1e-12)
+    # raising every group minimum by c adds f_d(c 1) = c * (row sums of W_d) before RoPE
+    c = 0.25
+    K2, V2 = oracle.restore(cfg, refs, q, zmin + c, delta, idx, Wd, np.array([1], np.int32))
+    shift = c * Wd.sum(axis=1)
+    assert np.allclose(V2[0] - V[0], shift[dk:], rtol=0, atol=1e-12)
+    for h in range(cfg.N):
+        s = slice(h * cfg.D, (h + 1) * cfg.D)
+        got = K2[0, s] - K[0, s]
+        assert np.allclose(got, oracle.rope(shift[:dk][s], 1.0, cfg.rope_base), rtol=0, atol=1e-12)
+    # the mean of the chosen references enters with weight 1/k_i
+    idx2 = idx.copy()
+    idx2[1, :2] = [0, 2]
+    K3, V3 = oracle.restore(cfg, refs, q, zmin, delta, idx2, Wd, np.array([1], np.int32))
+    refs2 = refs.copy()
+    refs2[0] += 1.0
+    K4, V4 = oracle.restore(cfg, refs2, q, zmin, delta, idx2, Wd, np.array([1], np.int32))
+    assert np.allclose(V4[0] - V3[0], 0.5, rtol=0, atol=1e-12)
