@@ -158,6 +158,25 @@ rkv_status rkv_gather_dequant(const rkv_params *p, const rkv_ref_pool *pool,
                               void *out_z, void *out_mean, int32_t out_dtype,
                               int32_t *dev_status, void *stream);
 
+/* Restore K and V of the selected tokens [RKV §2.5 = Sec. IV-B; §2.7 = Sec. IV-C]:
+ *   KV^_t = z~_t W_d + mean_t   (z~_t, mean_t as returned by rkv_gather_dequant),
+ *   K^_t = KV^_t[0, N D),  V^_t = KV^_t[N D, 2 N D),  head h = [h D, (h+1) D);
+ * every key head is rotated at the token's own position t (its index in the
+ * sequence; the restored key is pre-RoPE [RKV §2.1]): coordinate pairs (2i, 2i+1)
+ * by the angle t * rope_base^(-2i/D).  The page does not fix the RoPE variant; this
+ * is the rotary embedding as first defined, with consecutive pairs.
+ * Wd: [L][2 N D][d_c] out-major (Wd[c][j] = W_d[j][c]), bf16.
+ * sel: [L*B][n_sel] int32 token positions (-1: padding, zero rows; >= T or a stored
+ * slot >= n_ref: RKV_ERR_INDEX in dev_status and zero rows).
+ * out_k, out_v: bf16 [L*B][n_sel][N D].
+ * The decoder runs on the tensor cores with z~ rounded to bf16 and fp32 accumulation;
+ * the mean is an fp32 sum in ascending slot order times 1/k.
+ * Requires kv_dtype bf16, d_c in {256, 512}, 2 N D a multiple of 256, D a multiple
+ * of 32 and at most 256, rope_base > 0 (else RKV_ERR_UNSUPPORTED / _INVALID_ARG).    */
+rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const rkv_cache *cache,
+                          const void *Wd, const int32_t *sel, int32_t n_sel, double rope_base,
+                          void *out_k, void *out_v, int32_t *dev_status, void *stream);
+
 /* rkv_compress without a workspace argument: for callers that cannot allocate
  * device memory at the call site -- code running while a CUDA graph is captured
  * (cudaMalloc is not allowed there), runtimes whose device memory belongs to an

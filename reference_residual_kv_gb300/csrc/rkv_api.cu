@@ -32,6 +32,8 @@ Geometry make_geometry(const rkv_params *p)
     g.B = p->B;
     g.LB = p->L * p->B;
     g.T = p->T;
+    g.N = p->N;
+    g.D = p->D;
     g.W = 2 * p->N * p->D;
     g.d_ff = p->d_ff;
     g.d_c = p->d_c;
@@ -241,6 +243,31 @@ rkv_status rkv_gather_dequant(const rkv_params *p, const rkv_ref_pool *pool,
     if ((long long)g.LB * n_sel > (long long)INT_MAX) return RKV_ERR_UNSUPPORTED;
     cudaError_t e = launch_gather(g, pool, cache, sel, n_sel, out_z, out_mean, out_dtype,
                                   dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
+rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const rkv_cache *cache,
+                          const void *Wd, const int32_t *sel, int32_t n_sel, double rope_base,
+                          void *out_k, void *out_v, int32_t *dev_status, void *stream)
+{
+    rkv_status st = check_params(p);
+    if (st != RKV_OK) return st;
+    if (n_sel < 0 || !(rope_base > 0.0) || !isfinite(rope_base)) return RKV_ERR_INVALID_ARG;
+    if (p->kv_dtype != RKV_BF16) return RKV_ERR_UNSUPPORTED;
+    if ((p->d_c != 256 && p->d_c != 512) || (2 * p->N * p->D) % 256 != 0 || p->D % 32 != 0 ||
+        p->D > 256)
+        return RKV_ERR_UNSUPPORTED;
+    if ((st = check_pool(pool, make_geometry(p).n_ref)) != RKV_OK) return st;
+    if ((st = check_cache(cache)) != RKV_OK) return st;
+    if (n_sel == 0) return RKV_OK;
+    if (!Wd || !sel || !out_k || !out_v || !dev_status) return RKV_ERR_INVALID_ARG;
+    if (!aligned16(Wd) || !aligned16(sel) || !aligned16(out_k) || !aligned16(out_v) ||
+        !aligned16(dev_status))
+        return RKV_ERR_ALIGNMENT;
+    Geometry g = make_geometry(p);
+    if ((long long)g.LB * n_sel * g.W > (long long)INT_MAX * 64) return RKV_ERR_UNSUPPORTED;
+    cudaError_t e = launch_restore(g, pool, cache, Wd, sel, n_sel, rope_base, out_k, out_v,
+                                   dev_status, (cudaStream_t)stream);
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 

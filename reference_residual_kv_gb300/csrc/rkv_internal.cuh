@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cuda.h>
 #include <stdint.h>
 #include <stddef.h>
 
@@ -36,7 +37,7 @@ constexpr int kDistChunk = 8;             // N-tiles (2048 references) per dista
 constexpr long long kWaitCycles = 2000000000LL;
 
 struct Geometry {
-    int L, B, LB, T, W, d_ff, d_c, k, bits, n_ref, n_groups, code_pitch;
+    int L, B, LB, T, N, D, W, d_ff, d_c, k, bits, n_ref, n_groups, code_pitch;
     int kv_dtype, ref_dtype;
     int stride, first, n_sink;
     double alpha;
@@ -94,6 +95,16 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
 cudaError_t launch_token_norms(const Geometry &g, const void *kv, float *xnorm, cudaStream_t s);
 
 int device_sm_count();
+
+// bf16 [batch][rows][inner] tensor map, box = 64 (inner) x box_rows, 128-byte swizzle
+// (rkv_umma.cu); false if the driver rejects it.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+              uint64_t batch, uint32_t box_rows);
+
+// restore of K and V for selected tokens (rkv_restore.cu)
+cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
+                           const void *Wd, const int32_t *sel, int n_sel, double rope_base,
+                           void *out_k, void *out_v, int32_t *status, cudaStream_t s);
 
 // per-kernel event timing (rkv_prof.cu); no-ops unless rkv_profile_enable(1)
 void prof_begin(const char *name, cudaStream_t s);

@@ -1,0 +1,449 @@
+// rkv_restore.cu -- restore K and V of the tokens a decode step selects
+// [RKV §2.5 = Sec. IV-B, §2.7 = Sec. IV-C]:
+//   KV^_t = z~_t W_d + mean_t,  K^ = KV^[0, N D), V^ = KV^[N D, 2 N D),
+// z~_t = q delta + z_min (the token's own codes), mean_t = the mean of its stored
+// references, and each key head rotated at the token's own position t (the restored
+// key is pre-RoPE [RKV §2.1]): consecutive pairs (2i, 2i+1) by t * base^(-2i/D).
+//
+// One persistent kernel on CTA pairs issuing 2-SM MMAs (tcgen05.mma.cta_group::2,
+// M = 256 selected tokens x N = 256 output columns x K = 16, bf16 in, fp32 in TMEM):
+//   warp 0      TMA producer (both CTAs): this CTA's 128 rows of W_d (out-major) per
+//               64-wide K chunk; both CTAs' copies complete on the leader's barrier
+//   warp 1      TMEM allocation (both CTAs); MMA issue (leader)
+//   warps 2..9  per item (256 selected tokens of one layer-sequence): first write the
+//               CTA's 128 rows of z~ (dequantised codes, bf16) into shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads, resident for all N tiles;
+//               then, per N tile, read the accumulator, add the reference mean, rotate
+//               key pairs and store bf16.
+// Every mbarrier wait is bounded; on expiry the kernel reports RKV_ERR_DEVICE_TIMEOUT.
+#include "rkv_internal.cuh"
+#include "umma.cuh"
+
+#include <cuda_fp16.h>
+#include <math.h>
+#include <string.h>
+
+namespace rkv {
+namespace {
+
+constexpr int kEpi = 8;
+constexpr int kThr = 64 + 32 * kEpi;
+constexpr int kMaxDc = 512;                    // resident z~ tile: 128 rows x d_c bf16
+constexpr int kZBytes = kBM * kMaxDc * 2;      // 128 KB
+constexpr int kWBytes = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 W_d rows x 64
+constexpr int kStages = 5;
+constexpr int kSmem = kZBytes + kStages * kWBytes + 1024 + 256;
+constexpr int kMaxPairs = 128;                 // D <= 256
+
+struct RestoreArgs {
+    int LB, B, T, n_sel, W, dk, D, d_c, bits, n_ref, ref_fp8;
+    int tiles_t, n_tiles, k_chunks;
+    const int32_t *sel;
+    const uint8_t *codes;
+    const float2 *hdr;
+    const int4 *ref_idx;
+    const void *ref_vec;
+    __nv_bfloat16 *out_k, *out_v;
+    int32_t *status;
+    float2 theta[kMaxPairs];                   // base^(-2i/D) as hi + lo floats
+};
+
+// 2 pi = k2PiA + k2PiB + k2PiC (k2PiA has 8 significant bits, so kq * k2PiA is exact
+// for |kq| < 2^15, and the first reduction step is exact)
+constexpr float k2PiA = 6.28125f;
+constexpr float k2PiB = (float)(6.283185307179586476925 - 6.28125);
+constexpr float k2PiC = (float)(6.283185307179586476925 - 6.28125 - (double)(float)(6.283185307179586476925 - 6.28125));
+constexpr float kInv2Pi = 0.15915494309189533577f;
+
+// cos and sin of pos * theta, theta = hi + lo: the product is formed as a two-float sum
+// (the rounding error of pos * hi recovered with an fma), reduced modulo 2 pi with a
+// three-part 2 pi (Cody-Waite), then evaluated on |r| <= ~pi.
+__device__ __forceinline__ void rope_cs(float pos, float2 th, float &c, float &s)
+{
+    const float a_hi = pos * th.x;
+    const float a_lo = fmaf(pos, th.y, fmaf(pos, th.x, -a_hi));
+    const float kq = rintf(a_hi * kInv2Pi);
+    float r = fmaf(-kq, k2PiA, a_hi);
+    r = fmaf(-kq, k2PiB, r);
+    r = fmaf(-kq, k2PiC, r);
+    r += a_lo;
+    __sincosf(r, &s, &c);
+}
+
+// Dequantise one lane's coordinates of one token row and write them as bf16 into the
+// z~ tile: row r, coordinates [lane*cpl, (lane+1)*cpl), cpl = d_c/32 (8 or 16).
+// Layout: K chunk kc (64 coordinates) is a 128-row x 128-byte block at kc * 16 KB; the
+// 16-byte unit j (8 coordinates) of row r sits at unit position j ^ (r & 7).
+__device__ __forceinline__ void build_row(uint8_t *zt, int r, int lane, int d_c, int bits,
+                                          const uint8_t *crow, const float2 *hrow, bool ok)
+{
+    const int cpl = d_c >> 5;
+    const int c0 = lane * cpl;
+    float2 gh = make_float2(0.0f, 0.0f);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (ok) {
+        gh = __ldg(hrow + (c0 >> 5));
+        const int nbytes = cpl * bits / 8;      // 2, 4 or 8
+        const uint8_t *p = crow + c0 * bits / 8;
+        if (nbytes == 8) { const uint2 u = __ldg((const uint2 *)p); w[0] = u.x; w[1] = u.y; }
+        else if (nbytes == 4) w[0] = __ldg((const uint32_t *)p);
+        else w[0] = __ldg((const unsigned short *)p);
+    }
+#pragma unroll
+    for (int u8 = 0; u8 < 2; ++u8) {
+        if (u8 * 8 >= cpl) break;
+        __align__(16) __nv_bfloat162 o[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const int c = u8 * 8 + e;            // coordinate within the lane
+            int q0, q1;
+            if (bits == 4) {
+                q0 = (w[c >> 3] >> (4 * (c & 7))) & 15;
+                q1 = (w[(c + 1) >> 3] >> (4 * ((c + 1) & 7))) & 15;
+            } else {
+                q0 = (w[c >> 4] >> (2 * (c & 15))) & 3;
+                q1 = (w[(c + 1) >> 4] >> (2 * ((c + 1) & 15))) & 3;
+            }
+            const float z0 = ok ? fmaf((float)q0, gh.y, gh.x) : 0.0f;
+            const float z1 = ok ? fmaf((float)q1, gh.y, gh.x) : 0.0f;
+            o[e >> 1] = __float22bfloat162_rn(make_float2(z0, z1));
+        }
+        const int cc = c0 + u8 * 8;              // first coordinate of this unit
+        const int kc = cc >> 6, j = (cc & 63) >> 3;
+        *(uint4 *)(zt + kc * (kBM * 128) + r * 128 + ((j ^ (r & 7)) << 4)) = *(const uint4 *)o;
+    }
+}
+
+// Sum of the k references' values at 32 consecutive coordinates c0..c0+31 (fp32, slot
+// order) for one token; FP8 references decode exactly through fp16.
+__device__ __forceinline__ void ref_sum32(const RestoreArgs &a, const int (&slot)[4], int lb,
+                                          int c0, float (&m)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) m[j] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (slot[q] < 0) continue;
+        const size_t row = ((size_t)lb * a.n_ref + slot[q]) * a.W + c0;
+        if (a.ref_fp8) {
+            const uint4 *p = (const uint4 *)((const uint8_t *)a.ref_vec + row);
+            const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+            const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+                m[2 * e] += f.x;
+                m[2 * e + 1] += f.y;
+            }
+        } else {
+            const uint4 *p = (const uint4 *)((const __nv_bfloat16 *)a.ref_vec + row);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 u = __ldg(p + v);
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    m[v * 8 + 2 * e] += __uint_as_float(wv[e] << 16);
+                    m[v * 8 + 2 * e + 1] += __uint_as_float(wv[e] & 0xffff0000u);
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThr, 1)
+k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ RestoreArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *zt = smem_raw + ((1024u - (um::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *wst = zt + kZBytes;                                  // W_d stages
+    uint64_t *full = (uint64_t *)(wst + kStages * kWBytes);       // leader's: both CTAs' bytes
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;                                  // leader's: both epilogues
+    uint64_t *zready = tempty + 2;                                 // leader's: both z~ tiles
+    uint64_t *drain = zready + 1;
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = um::cluster_rank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            um::mbar_init(&full[s], 1);
+            um::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            um::mbar_init(&tfull[b], 1);
+            um::mbar_init(&tempty[b], 2 * kEpi);
+        }
+        um::mbar_init(zready, 2 * kEpi);
+        um::mbar_init(drain, 1);
+        *abort_flag = 0;
+        um::fence_mbar_init();
+    }
+    if (warp == 1) {
+        um::tmem_alloc2(tmem_slot, 512);
+        um::tmem_relinquish2();
+    }
+    um::tc_fence_before();
+    um::cluster_sync();
+    um::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_items = a.LB * a.tiles_t;
+    const int pid = blockIdx.x / 2, npairs = gridDim.x / 2;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            um::prefetch_tmap(&tmW);
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t last_ph[kStages];
+            bool used[kStages];
+            for (int s = 0; s < kStages; ++s) { used[s] = false; last_ph[s] = 0; }
+            bool ok = true;
+            for (int i = pid; i < n_items && ok; i += npairs) {
+                const int lz = (i / a.tiles_t) / a.B;
+                for (int n = 0; n < a.n_tiles && ok; ++n) {
+                    for (int kc = 0; kc < a.k_chunks; ++kc) {
+                        const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles);
+                        if (*abort_flag || !w) { ok = false; break; }
+                        const uint32_t fb = um::smem_u32(&full[stage]);
+                        if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kWBytes);
+                        um::tma_load_3d_pair(wst + stage * kWBytes, &tmW, leader ? fb : um::mapa(fb, 0),
+                                             kc * kBK, n * kBN + (int)rank * (kBN / 2), lz);
+                        used[stage] = true;
+                        last_ph[stage] = ph;
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            for (int s = 0; s < kStages; ++s)
+                if (used[s]) um::mbar_wait(&empty[s], last_ph[s], kWaitCycles);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0, cnt = 0, ic = 0;
+            bool ok = true;
+            const uint32_t idesc = um::idesc_bf16_f32(2 * kBM, kBN);
+            const uint32_t zbase = um::smem_u32(zt);
+            for (int i = pid; i < n_items && ok; i += npairs, ++ic) {
+                // both CTAs' z~ tiles of this item are written
+                const bool wz = um::mbar_wait(zready, ic & 1u, kWaitCycles);
+                if (*abort_flag || !wz) { ok = false; break; }
+                um::tc_fence_after();
+                for (int n = 0; n < a.n_tiles && ok; ++n) {
+                    const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
+                    const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles);
+                    if (*abort_flag || !w) { ok = false; break; }
+                    um::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kBN;
+                    for (int kc = 0; kc < a.k_chunks; ++kc) {
+                        const bool wf = um::mbar_wait(&full[stage], ph, kWaitCycles);
+                        if (*abort_flag || !wf) { ok = false; break; }
+                        um::tc_fence_after();
+                        const uint64_t ad = um::sdesc_sw128(zbase + kc * (kBM * 128));
+                        const uint64_t bd = um::sdesc_sw128(um::smem_u32(wst + stage * kWBytes));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)
+                            um::mma2_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
+                        um::mma2_commit_mc(&empty[stage], 3);
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    um::mma2_commit_mc(&tfull[buf], 3);
+                    ++cnt;
+                }
+            }
+            if (!ok) {
+                set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            um::mma2_commit_mc(drain, 1);
+            um::mbar_wait(drain, 0, kWaitCycles);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const int row = q * 32 + lane;                      // TMEM lane = z~ row
+        const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+        const uint32_t zready_l = um::smem_u32(zready);
+        uint32_t cnt = 0;
+        bool ok = true;
+        for (int i = pid; i < n_items; i += npairs) {
+            const int lb = i / a.tiles_t, t = i % a.tiles_t;
+            const int e0 = t * 2 * kBM + (int)rank * kBM;   // this CTA's first selected entry
+            // (1) this warp's 16 rows of the CTA's z~ tile
+            for (int rr = 0; rr < kBM / kEpi; ++rr) {
+                const int r = (warp - 2) * (kBM / kEpi) + rr;
+                const int e = e0 + r;
+                const int tok = e < a.n_sel ? __ldg(a.sel + (size_t)lb * a.n_sel + e) : -1;
+                const bool okr = tok >= 0 && tok < a.T;
+                const size_t rec = (size_t)lb * a.T + (okr ? tok : 0);
+                build_row(zt, r, lane, a.d_c, a.bits, a.codes + rec * (size_t)(a.d_c * a.bits / 8),
+                          a.hdr + rec * (a.d_c / 32), okr);
+            }
+            um::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) um::mbar_arrive(zready);
+                else um::mbar_arrive_cluster(um::mapa(zready_l, 0));
+            }
+            // (2) this thread's token: position, reference slots, 1/k
+            const int e = e0 + row;
+            int tok = e < a.n_sel ? __ldg(a.sel + (size_t)lb * a.n_sel + e) : -1;
+            if (tok >= a.T) set_status(a.status, RKV_ERR_INDEX);
+            bool okt = tok >= 0 && tok < a.T;
+            int slot[4] = {-1, -1, -1, -1};
+            int kk = 0;
+            if (okt) {
+                const int4 ix = __ldg(a.ref_idx + (size_t)lb * a.T + tok);
+                slot[0] = ix.x; slot[1] = ix.y; slot[2] = ix.z; slot[3] = ix.w;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (slot[j] >= a.n_ref) { okt = false; set_status(a.status, RKV_ERR_INDEX); }
+                    if (slot[j] >= 0) ++kk;
+                }
+            }
+            const float inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
+            const float pos = (float)(okt ? tok : 0);
+            const size_t orow = (size_t)lb * a.n_sel + e;
+            // (3) the N tiles' accumulators
+            for (int n = 0; n < a.n_tiles; ++n) {
+                const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
+                bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                um::tc_fence_after();
+                const uint32_t tb = tl + buf * kBN;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int col = h * (kBN / 2) + cc * 32;          // column within the tile
+                    const int c0 = n * kBN + col;                     // output coordinate
+                    float v[32];
+                    um::tmem_ld32(tb + col, v);
+                    if (e >= a.n_sel) continue;
+                    const bool is_k = c0 < a.dk;
+                    __nv_bfloat16 *dst = (is_k ? a.out_k + orow * a.dk + c0 : a.out_v + orow * a.dk + (c0 - a.dk));
+                    float o[32];
+                    if (okt) {
+                        float m[32];
+                        ref_sum32(a, slot, lb, c0, m);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = fmaf(m[j], inv_k, v[j]);
+                        if (is_k) {
+                            const int p0 = (c0 % a.D) >> 1;           // first pair index
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                float cs, sn;
+                                rope_cs(pos, a.theta[p0 + j], cs, sn);
+                                const float x0 = o[2 * j], x1 = o[2 * j + 1];
+                                o[2 * j] = x0 * cs - x1 * sn;
+                                o[2 * j + 1] = x0 * sn + x1 * cs;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            pk[j] = __float22bfloat162_rn(make_float2(o[8 * u + 2 * j], o[8 * u + 2 * j + 1]));
+                        *(uint4 *)(dst + 8 * u) = *(const uint4 *)pk;
+                    }
+                }
+                um::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) um::mbar_arrive_relaxed(&tempty[buf]);
+                    else um::mbar_arrive_cluster_relaxed(um::mapa(um::smem_u32(&tempty[buf]), 0));
+                }
+                ++cnt;
+            }
+            if (!ok) break;
+        }
+        if (!ok) {
+            set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+
+    um::tc_fence_before();
+    um::cluster_sync();
+    if (warp == 1) {
+        um::tc_fence_after();
+        um::tmem_dealloc2(tmem_base, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
+                           const void *Wd, const int32_t *sel, int n_sel, double rope_base,
+                           void *out_k, void *out_v, int32_t *status, cudaStream_t s)
+{
+    RestoreArgs a;
+    memset((void *)&a, 0, sizeof(a));
+    a.LB = g.LB; a.B = g.B; a.T = g.T; a.n_sel = n_sel; a.W = g.W; a.dk = g.W / 2;
+    a.D = g.D; a.d_c = g.d_c; a.bits = g.bits; a.n_ref = g.n_ref;
+    a.ref_fp8 = g.ref_dtype == RKV_FP8_E4M3;
+    a.tiles_t = (n_sel + kTileM - 1) / kTileM;
+    a.n_tiles = g.W / kBN;
+    a.k_chunks = g.d_c / kBK;
+    a.sel = sel; a.codes = cache->codes; a.hdr = (const float2 *)cache->hdr;
+    a.ref_idx = (const int4 *)cache->ref_idx; a.ref_vec = pool->ref_vec;
+    a.out_k = (__nv_bfloat16 *)out_k; a.out_v = (__nv_bfloat16 *)out_v; a.status = status;
+    for (int i = 0; i < a.D / 2; ++i) {
+        const double th = pow(rope_base, -2.0 * (double)i / (double)a.D);
+        const float hi = (float)th;
+        a.theta[i] = make_float2(hi, (float)(th - (double)hi));
+    }
+    CUtensorMap mW;
+    if (!make_map(&mW, Wd, g.d_c, g.W, g.L, kBN / 2)) return cudaErrorInvalidValue;
+
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_restore, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const long long items = (long long)g.LB * a.tiles_t;
+    if (items <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThr, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    static int max_pairs = 0;
+    if (max_pairs == 0) {
+        cfg.gridDim = dim3(2 * 64, 1, 1);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)k_restore, &cfg);
+        if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
+    }
+    const long long np = items < max_pairs ? items : max_pairs;
+    cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
+    ProfScope prof("restore_kv", s);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_restore, mW, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace rkv

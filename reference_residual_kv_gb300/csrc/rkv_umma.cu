@@ -554,8 +554,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // bf16 [batch][rows][inner] row-major, box = 64 (inner) x box_rows, 128-byte swizzle.
-static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
-                     uint64_t batch, uint32_t box_rows)
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+              uint64_t batch, uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return false;

@@ -203,6 +203,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Make this thread's shared-memory writes visible to the async proxy (tensor-core
+// operand reads) before a synchronisation that hands them over.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- CTA pairs (2-SM MMA) ---------------------------------------------------------
 // The shared::cluster address of the object at local shared address `a` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa(uint32_t a, uint32_t rank)

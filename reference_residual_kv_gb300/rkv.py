@@ -17,7 +17,7 @@ RKV_F32, RKV_BF16, RKV_FP8_E4M3 = 0, 1, 2
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_ALIGNMENT = 0, 1, 2, 3
 RKV_ERR_CUDA, RKV_ERR_INDEX, RKV_ERR_DEVICE_TIMEOUT, RKV_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("rkv_n_ref", "rkv_query_sizes", "rkv_build_ref_pool", "rkv_compress",
-            "rkv_gather_dequant", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
+            "rkv_gather_dequant", "rkv_restore_kv", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
             "rkv_status_string")
 _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 
@@ -73,6 +73,9 @@ def lib():
         L.rkv_gather_dequant.argtypes = [P, ctypes.POINTER(rkv_ref_pool), ctypes.POINTER(rkv_cache),
                                          V, I32, V, V, I32, V, V]
         L.rkv_gather_dequant.restype = I32
+        L.rkv_restore_kv.argtypes = [P, ctypes.POINTER(rkv_ref_pool), ctypes.POINTER(rkv_cache),
+                                     V, V, I32, ctypes.c_double, V, V, V, V]
+        L.rkv_restore_kv.restype = I32
         L.rkv_profile_enable.argtypes = [I32]
         L.rkv_profile_enable.restype = I32
         L.rkv_profile_collect.argtypes = [ctypes.c_char_p, I32, ctypes.POINTER(ctypes.c_float),
@@ -167,6 +170,15 @@ def rkv_gather_dequant(p: rkv_params, pool: rkv_ref_pool, cache: rkv_cache, sel,
         raise RkvError(st, "rkv_gather_dequant")
 
 
+def rkv_restore_kv(p: rkv_params, pool: rkv_ref_pool, cache: rkv_cache, Wd, sel, n_sel: int,
+                   rope_base: float, out_k, out_v, dev_status, stream=None) -> None:
+    st = lib().rkv_restore_kv(ctypes.byref(p), ctypes.byref(pool), ctypes.byref(cache), _ptr(Wd),
+                              _ptr(sel), int(n_sel), float(rope_base), _ptr(out_k), _ptr(out_v),
+                              _ptr(dev_status), _stream(stream))
+    if st:
+        raise RkvError(st, "rkv_restore_kv")
+
+
 def rkv_profile_enable(on: bool) -> None:
     lib().rkv_profile_enable(1 if on else 0)
 
@@ -232,6 +244,10 @@ class Buffers:
             out_dtype = RKV_F32 if out_z.dtype == torch.float32 else RKV_BF16
         rkv_gather_dequant(self.p, self.pool, self.cache, sel, n_sel, out_z, out_mean, out_dtype,
                            self.status, stream)
+
+    def restore(self, Wd, sel, out_k, out_v, rope_base: float, stream=None):
+        rkv_restore_kv(self.p, self.pool, self.cache, Wd, sel, sel.shape[-1], rope_base, out_k,
+                       out_v, self.status, stream)
 
     def device_status(self) -> int:
         return int(self.status[0].item())

@@ -104,3 +104,23 @@ def test_dynamic_schedule_rejects_non_advancing_first_step(lib):
     assert rkv.rkv_n_ref(p) == -1
     a = ctypes.c_size_t()
     assert lib.rkv_query_sizes(ctypes.byref(p), ctypes.byref(a), None, None) == rkv.RKV_ERR_INVALID_ARG
+
+
+def test_restore_validates_on_the_host(lib):
+    pool = rkv.rkv_ref_pool(16, 16, 16, 16, 16)
+    cache = rkv.rkv_cache(16, 16, 16)
+
+    def call(p, Wd=16, sel=16, n_sel=4, base=10000.0, ok=16, ov=16, st=16):
+        return lib.rkv_restore_kv(ctypes.byref(p), ctypes.byref(pool), ctypes.byref(cache), Wd, sel,
+                                  n_sel, base, ok, ov, st, None)
+
+    p = rkv.make_params(1, 1, 256, 8, 128, 1024, 512)
+    assert call(p, n_sel=-1) == rkv.RKV_ERR_INVALID_ARG
+    assert call(p, base=0.0) == rkv.RKV_ERR_INVALID_ARG
+    assert call(p, base=float("inf")) == rkv.RKV_ERR_INVALID_ARG
+    assert call(p, Wd=None) == rkv.RKV_ERR_INVALID_ARG
+    assert call(p, ok=24) == rkv.RKV_ERR_ALIGNMENT
+    assert call(p, n_sel=0) == rkv.RKV_OK                     # nothing to do, nothing launched
+    assert call(rkv.make_params(1, 1, 256, 2, 64, 256, 64, kv_dtype="f32")) == rkv.RKV_ERR_UNSUPPORTED
+    assert call(rkv.make_params(1, 1, 256, 8, 128, 1024, 384)) == rkv.RKV_ERR_UNSUPPORTED   # d_c
+    assert call(rkv.make_params(1, 1, 256, 2, 48, 1024, 512)) == rkv.RKV_ERR_UNSUPPORTED    # D
