@@ -96,6 +96,13 @@ def algorithmic(cfg: wl.Config):
     return fl, n_ref, n_non, pairs
 
 
+def restore_bytes_per_token(cfg, out_bytes=2):
+    """Algorithmic HBM bytes of restoring one selected token: its codes, group extremes,
+    reference slots and index, and the K and V rows written (the pool and W_d are read
+    once per call and stay in L2)."""
+    return cfg.d_c * cfg.bits // 8 + (cfg.d_c // 32) * 8 + 16 + 4 + cfg.W * out_bytes
+
+
 def gather_bytes_per_token(cfg, out_bytes=2):
     return (cfg.d_c * cfg.bits // 8 + (cfg.d_c // 32) * 8 + 16 + 4 + cfg.d_c * out_bytes
             + cfg.W * out_bytes)
@@ -278,6 +285,37 @@ def read_path(dev, steps=256, reps=3):
     ms = a.elapsed_time(b) / (reps * steps)
     st = bufs.device_status()
     n_tok = sum(x.numel() for x in sels) / steps
+    # restore (decoder + mean + RoPE) of the same selections, fewer steps per graph
+    r_steps = min(32, steps)
+    Wd = torch.from_numpy(wl.decoder_weights(cfg, 0)[None].view(np.int16)).view(torch.bfloat16).to(dev)
+    dk = cfg.N * cfg.D
+    ok_ = torch.empty((1, nmax, dk), dtype=torch.bfloat16, device=dev)
+    ov_ = torch.empty_like(ok_)
+    with torch.cuda.stream(side):
+        for s_ in sels[:2]:
+            bufs.restore(Wd, s_.view(1, -1), ok_, ov_, cfg.rope_base, stream=side)
+    side.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=side):
+        for s_ in sels[:r_steps]:
+            bufs.restore(Wd, s_.view(1, -1), ok_, ov_, cfg.rope_base, stream=side)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(reps):
+        gr.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    r_ms = a.elapsed_time(b) / (reps * r_steps)
+    r_tok = sum(x.numel() for x in sels[:r_steps]) / r_steps
+    r_flops = 2.0 * r_tok * cfg.d_c * cfg.W
+    r_bytes = r_tok * restore_bytes_per_token(cfg) + bufs.n_ref * cfg.W * 1
+    _, tf_burst, tf_sust, _ = _peaks()
+    restore = {"tokens_per_s": r_tok / (r_ms / 1e3), "ms_per_step": r_ms, "steps": r_steps,
+               "flops_per_step": r_flops, "achieved_tflops": r_flops / (r_ms / 1e3) / 1e12,
+               "frac_of_sustained": r_flops / (r_ms / 1e3) / 1e12 / tf_sust,
+               "bytes_per_step": r_bytes, "achieved_gbs": r_bytes / (r_ms / 1e3) / 1e9,
+               "device_status": bufs.device_status()}
     per_tok = gather_bytes_per_token(cfg)
     ref_bytes = bufs.n_ref * cfg.W * 1
     bytes_step = n_tok * per_tok + ref_bytes
@@ -291,7 +329,7 @@ def read_path(dev, steps=256, reps=3):
             "unit": "GB/s", "frac": gbs / hbm, "peak_source": "%s HBM copy bandwidth" % src,
             "device_status": st,
             "compress_tokens_per_s": cfg.T / (c_ms / 1e3), "compress_ms": c_ms,
-            "compress_kernels_ms": c_prof}
+            "compress_kernels_ms": c_prof, "restore": restore}
 
 
 def run_ours(args, cfg):

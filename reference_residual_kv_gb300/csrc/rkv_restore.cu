@@ -70,25 +70,40 @@ __device__ __forceinline__ void rope_cs(float pos, float2 th, float &c, float &s
     __sincosf(r, &s, &c);
 }
 
-// Dequantise one lane's coordinates of one token row and write them as bf16 into the
-// z~ tile: row r, coordinates [lane*cpl, (lane+1)*cpl), cpl = d_c/32 (8 or 16).
-// Layout: K chunk kc (64 coordinates) is a 128-row x 128-byte block at kc * 16 KB; the
-// 16-byte unit j (8 coordinates) of row r sits at unit position j ^ (r & 7).
-__device__ __forceinline__ void build_row(uint8_t *zt, int r, int lane, int d_c, int bits,
-                                          const uint8_t *crow, const float2 *hrow, bool ok)
+// One lane's share of a token row of z~: coordinates [lane*cpl, (lane+1)*cpl),
+// cpl = d_c/32 (8 or 16): its code words and its group's {z_min, delta}.
+struct RowCodes {
+    uint32_t w0, w1;
+    float2 gh;
+};
+
+__device__ __forceinline__ RowCodes load_row(int lane, int d_c, int bits, const uint8_t *crow,
+                                             const float2 *hrow, bool ok)
+{
+    RowCodes rc = {0u, 0u, make_float2(0.0f, 0.0f)};
+    if (ok) {
+        const int cpl = d_c >> 5;
+        const int c0 = lane * cpl;
+        rc.gh = __ldg(hrow + (c0 >> 5));
+        const int nbytes = cpl * bits / 8;      // 2, 4 or 8
+        const uint8_t *p = crow + c0 * bits / 8;
+        if (nbytes == 8) { const uint2 u = __ldg((const uint2 *)p); rc.w0 = u.x; rc.w1 = u.y; }
+        else if (nbytes == 4) rc.w0 = __ldg((const uint32_t *)p);
+        else rc.w0 = __ldg((const unsigned short *)p);
+    }
+    return rc;
+}
+
+// Dequantise a lane's share (z~ = q delta + z_min, one fma) and write it as bf16 into
+// the z~ tile, row r.  Layout: K chunk kc (64 coordinates) is a 128-row x 128-byte block
+// at kc * 16 KB; the 16-byte unit j (8 coordinates) of row r sits at unit j ^ (r & 7).
+// Rows that are not restored (padding, bad index) are written as zeros.
+__device__ __forceinline__ void write_row(uint8_t *zt, int r, int lane, int d_c, int bits,
+                                          const RowCodes &rc, bool ok)
 {
     const int cpl = d_c >> 5;
     const int c0 = lane * cpl;
-    float2 gh = make_float2(0.0f, 0.0f);
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (ok) {
-        gh = __ldg(hrow + (c0 >> 5));
-        const int nbytes = cpl * bits / 8;      // 2, 4 or 8
-        const uint8_t *p = crow + c0 * bits / 8;
-        if (nbytes == 8) { const uint2 u = __ldg((const uint2 *)p); w[0] = u.x; w[1] = u.y; }
-        else if (nbytes == 4) w[0] = __ldg((const uint32_t *)p);
-        else w[0] = __ldg((const unsigned short *)p);
-    }
+    const uint32_t w[2] = {rc.w0, rc.w1};
 #pragma unroll
     for (int u8 = 0; u8 < 2; ++u8) {
         if (u8 * 8 >= cpl) break;
@@ -104,8 +119,8 @@ __device__ __forceinline__ void build_row(uint8_t *zt, int r, int lane, int d_c,
                 q0 = (w[c >> 4] >> (2 * (c & 15))) & 3;
                 q1 = (w[(c + 1) >> 4] >> (2 * ((c + 1) & 15))) & 3;
             }
-            const float z0 = ok ? fmaf((float)q0, gh.y, gh.x) : 0.0f;
-            const float z1 = ok ? fmaf((float)q1, gh.y, gh.x) : 0.0f;
+            const float z0 = ok ? fmaf((float)q0, rc.gh.y, rc.gh.x) : 0.0f;
+            const float z1 = ok ? fmaf((float)q1, rc.gh.y, rc.gh.x) : 0.0f;
             o[e >> 1] = __float22bfloat162_rn(make_float2(z0, z1));
         }
         const int cc = c0 + u8 * 8;              // first coordinate of this unit
@@ -114,44 +129,57 @@ __device__ __forceinline__ void build_row(uint8_t *zt, int r, int lane, int d_c,
     }
 }
 
-// Sum of the k references' values at 32 consecutive coordinates c0..c0+31 (fp32, slot
-// order) for one token; FP8 references decode exactly through fp16.
-__device__ __forceinline__ void ref_sum32(const RestoreArgs &a, const int (&slot)[4], int lb,
-                                          int c0, float (&m)[32])
-{
+// The stored bytes of the k references' values at 32 consecutive coordinates of one
+// token (FP8: 32 bytes, bf16: 64 bytes per reference), loaded ahead of their use.
+template <bool FP8> struct RefChunk {
+    static constexpr int kU = FP8 ? 2 : 4;      // uint4 per reference
+    uint4 u[4][kU];
+
+    __device__ __forceinline__ void load(const RestoreArgs &a, const int (&slot)[4], int lb, int c0)
+    {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) m[j] = 0.0f;
+        for (int q = 0; q < 4; ++q) {
+            if (slot[q] < 0) continue;
+            const size_t row = ((size_t)lb * a.n_ref + slot[q]) * a.W + c0;
+            const uint4 *p = FP8 ? (const uint4 *)((const uint8_t *)a.ref_vec + row)
+                                 : (const uint4 *)((const __nv_bfloat16 *)a.ref_vec + row);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (slot[q] < 0) continue;
-        const size_t row = ((size_t)lb * a.n_ref + slot[q]) * a.W + c0;
-        if (a.ref_fp8) {
-            const uint4 *p = (const uint4 *)((const uint8_t *)a.ref_vec + row);
-            const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-            const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            for (int v = 0; v < kU; ++v) u[q][v] = __ldg(p + v);
+        }
+    }
+
+    // fp32 sum in ascending slot order; FP8 decodes exactly through fp16
+    __device__ __forceinline__ void sum(const int (&slot)[4], float (&m)[32]) const
+    {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-                const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-                m[2 * e] += f.x;
-                m[2 * e + 1] += f.y;
-            }
-        } else {
-            const uint4 *p = (const uint4 *)((const __nv_bfloat16 *)a.ref_vec + row);
+        for (int j = 0; j < 32; ++j) m[j] = 0.0f;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 u = __ldg(p + v);
-                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+        for (int q = 0; q < 4; ++q) {
+            if (slot[q] < 0) continue;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    m[v * 8 + 2 * e] += __uint_as_float(wv[e] << 16);
-                    m[v * 8 + 2 * e + 1] += __uint_as_float(wv[e] & 0xffff0000u);
+            for (int v = 0; v < kU; ++v) {
+                const uint32_t wv[4] = {u[q][v].x, u[q][v].y, u[q][v].z, u[q][v].w};
+                if (FP8) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+                        m[v * 16 + 2 * e] += f.x;
+                        m[v * 16 + 2 * e + 1] += f.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        m[v * 8 + 2 * e] += __uint_as_float(wv[e] << 16);
+                        m[v * 8 + 2 * e + 1] += __uint_as_float(wv[e] & 0xffff0000u);
+                    }
                 }
             }
         }
     }
-}
+};
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThr, 1)
 k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ RestoreArgs a)
 {
@@ -283,16 +311,26 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
         for (int i = pid; i < n_items; i += npairs) {
             const int lb = i / a.tiles_t, t = i % a.tiles_t;
             const int e0 = t * 2 * kBM + (int)rank * kBM;   // this CTA's first selected entry
-            // (1) this warp's 16 rows of the CTA's z~ tile
-            for (int rr = 0; rr < kBM / kEpi; ++rr) {
-                const int r = (warp - 2) * (kBM / kEpi) + rr;
-                const int e = e0 + r;
-                const int tok = e < a.n_sel ? __ldg(a.sel + (size_t)lb * a.n_sel + e) : -1;
-                const bool okr = tok >= 0 && tok < a.T;
-                const size_t rec = (size_t)lb * a.T + (okr ? tok : 0);
-                build_row(zt, r, lane, a.d_c, a.bits, a.codes + rec * (size_t)(a.d_c * a.bits / 8),
-                          a.hdr + rec * (a.d_c / 32), okr);
+            // (1) this warp's 16 rows of the CTA's z~ tile: every load first (the rows'
+            // positions, then their codes and extremes), then dequantise and write
+            constexpr int kRows = kBM / kEpi;
+            const int rbase = (warp - 2) * kRows;
+            int tsel = -1;
+            if (lane < kRows && e0 + rbase + lane < a.n_sel)
+                tsel = __ldg(a.sel + (size_t)lb * a.n_sel + e0 + rbase + lane);
+            RowCodes rcs[kRows];
+            bool okr[kRows];
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) {
+                const int tok = __shfl_sync(0xffffffffu, tsel, rr);
+                okr[rr] = tok >= 0 && tok < a.T;
+                const size_t rec = (size_t)lb * a.T + (okr[rr] ? tok : 0);
+                rcs[rr] = load_row(lane, a.d_c, a.bits, a.codes + rec * (size_t)(a.d_c * a.bits / 8),
+                                   a.hdr + rec * (a.d_c / 32), okr[rr]);
             }
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr)
+                write_row(zt, rbase + rr, lane, a.d_c, a.bits, rcs[rr], okr[rr]);
             um::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -318,7 +356,11 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
             const float inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
             const float pos = (float)(okt ? tok : 0);
             const size_t orow = (size_t)lb * a.n_sel + e;
-            // (3) the N tiles' accumulators
+            // (3) the N tiles' accumulators; the next chunk's reference values are
+            // loaded while this chunk is rotated and stored
+            RefChunk<FP8> rch;
+            const int n_chunks = a.n_tiles * 4;
+            if (okt) rch.load(a, slot, lb, h * (kBN / 2));
             for (int n = 0; n < a.n_tiles; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
                 bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
@@ -329,17 +371,22 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                 for (int cc = 0; cc < 4; ++cc) {
                     const int col = h * (kBN / 2) + cc * 32;          // column within the tile
                     const int c0 = n * kBN + col;                     // output coordinate
-                    float v[32];
-                    um::tmem_ld32(tb + col, v);
+                    float o[32];
+                    um::tmem_ld32(tb + col, o);
+                    if (okt) {
+                        // KV^ = f_d(z~) + (sum of the references) * 1/k
+                        float m[32];
+                        rch.sum(slot, m);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = fmaf(m[j], inv_k, o[j]);
+                    }
+                    const int g1 = n * 4 + cc + 1;
+                    if (okt && g1 < n_chunks)
+                        rch.load(a, slot, lb, (g1 >> 2) * kBN + h * (kBN / 2) + (g1 & 3) * 32);
                     if (e >= a.n_sel) continue;
                     const bool is_k = c0 < a.dk;
                     __nv_bfloat16 *dst = (is_k ? a.out_k + orow * a.dk + c0 : a.out_v + orow * a.dk + (c0 - a.dk));
-                    float o[32];
                     if (okt) {
-                        float m[32];
-                        ref_sum32(a, slot, lb, c0, m);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = fmaf(m[j], inv_k, v[j]);
                         if (is_k) {
                             const int p0 = (c0 % a.D) >> 1;           // first pair index
 #pragma unroll
@@ -413,11 +460,12 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     CUtensorMap mW;
     if (!make_map(&mW, Wd, g.d_c, g.W, g.L, kBN / 2)) return cudaErrorInvalidValue;
 
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_restore, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    auto kern = a.ref_fp8 ? k_restore<true> : k_restore<false>;
+    static bool attr[2] = {false, false};
+    if (!attr[a.ref_fp8]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[a.ref_fp8] = true;
     }
     const long long items = (long long)g.LB * a.tiles_t;
     if (items <= 0) return cudaSuccess;
@@ -435,13 +483,13 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     static int max_pairs = 0;
     if (max_pairs == 0) {
         cfg.gridDim = dim3(2 * 64, 1, 1);
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)k_restore, &cfg);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)kern, &cfg);
         if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
     }
     const long long np = items < max_pairs ? items : max_pairs;
     cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
     ProfScope prof("restore_kv", s);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_restore, mW, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
