@@ -323,3 +323,18 @@ def restore(cfg: wl.Config, refs64, q, zmin, delta, idx, Wd64, sel):
                        prf, pq, pmn, pdl, pidx, pw, psel, n, ko.ctypes.data_as(_dp),
                        vo.ctypes.data_as(_dp))
     return ko, vo
+
+
+def attention(q, K, V, N: int, valid=None) -> np.ndarray:
+    """Sparse attention of one decode step: q [H][D], K/V [n][N*D] -> o [H][D]."""
+    q, pq = _d(q)
+    K, pk = _d(K)
+    V, pv = _d(V)
+    H, D = q.shape
+    n = K.shape[0]
+    if valid is None:
+        valid = np.ones(n, np.int32)
+    valid, pva = _i(np.asarray(valid, np.int32))
+    o = np.zeros((H, D))
+    lib().rkvo_attention(H, N, D, pq, pk, pv, pva, n, o.ctypes.data_as(_dp))
+    return o

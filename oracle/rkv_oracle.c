@@ -431,3 +431,38 @@ void rkvo_restore(int N, int D, int d_c, int group, int k, double rope_base,
     }
     free(zq); free(mean); free(dec);
 }
+
+/* §2.7 = Sec. IV-C, sparse attention of one decode step over the restored set:
+ *   o_j = softmax( q_j K^_I^T / sqrt(D) ) V^_I
+ * for each query head j.  Reading (the page writes the formula per head): H query
+ * heads share the N key/value heads in groups of H/N, query head j reading KV head
+ * floor(j / (H/N)).  Rows n with valid[n] == 0 (padding) are not part of I.
+ * q [H][D]; K, V [n][N D] (head h = [h D, (h+1) D)); o [H][D].  The softmax is taken
+ * as exp(s - max s) / sum exp(s - max s), which equals the definition.            */
+void rkvo_attention(int H, int N, int D, const double *q, const double *K, const double *V,
+                    const int32_t *valid, int n, double *o)
+{
+    int G = H / N;
+    double *s = malloc(sizeof(double) * (n > 0 ? n : 1));
+    for (int j = 0; j < H; j++) {
+        int h = j / G;
+        double mx = -INFINITY;
+        for (int t = 0; t < n; t++) {
+            if (!valid[t]) continue;
+            double d = 0.0;
+            for (int c = 0; c < D; c++) d += q[(size_t)j * D + c] * K[(size_t)t * N * D + (size_t)h * D + c];
+            s[t] = d / sqrt((double)D);
+            if (s[t] > mx) mx = s[t];
+        }
+        double den = 0.0;
+        for (int t = 0; t < n; t++)
+            if (valid[t]) den += exp(s[t] - mx);
+        for (int c = 0; c < D; c++) {
+            double acc = 0.0;
+            for (int t = 0; t < n; t++)
+                if (valid[t]) acc += exp(s[t] - mx) * V[(size_t)t * N * D + (size_t)h * D + c];
+            o[(size_t)j * D + c] = den > 0.0 ? acc / den : 0.0;
+        }
+    }
+    free(s);
+}

@@ -36,6 +36,11 @@ MUTANTS = {
     "decoder weights transposed": ("s += z[j] * Wd[(size_t)c * d_c + j];", "s += z[j] * Wd[(size_t)j * W + c];"),
     "keys take the value half of the decoder": ("ko[c] = dec[c] + mean[c];", "ko[c] = dec[dk + c] + mean[c];"),
     "value without the reference mean": ("vo[c] = dec[dk + c] + mean[dk + c];", "vo[c] = dec[dk + c];"),
+    "attention scaled by 1/D": ("s[t] = d / sqrt((double)D);", "s[t] = d / (double)D;"),
+    "query heads mapped round-robin": ("int h = j / G;", "int h = j % N;"),
+    "padding rows attended": ("if (valid[t]) den += exp(s[t] - mx);", "den += exp(s[t] - mx);"),
+    "attention reads keys as values": ("acc += exp(s[t] - mx) * V[(size_t)t * N * D + (size_t)h * D + c];",
+                                       "acc += exp(s[t] - mx) * K[(size_t)t * N * D + (size_t)h * D + c];"),
 }
 
 

@@ -449,3 +449,53 @@ def test_restore_moves_only_keys_with_position_and_is_affine_in_the_minima():
     refs2[0] += 1.0
     K4, V4 = oracle.restore(cfg, refs2, q, zmin, delta, idx2, Wd, np.array([1], np.int32))
     assert np.allclose(V4[0] - V3[0], 0.5, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ sparse attention
+def test_attention_closed_forms():
+    rng = np.random.default_rng(9)
+    D, N = 8, 2
+    V = rng.standard_normal((5, N * D))
+    K = rng.standard_normal((5, N * D))
+    # uniform scores (q = 0): the mean of the selected values, per KV head
+    o = oracle.attention(np.zeros((4, D)), K, V, N)
+    for j in range(4):
+        h = j // 2
+        assert np.allclose(o[j], V[:, h * D:(h + 1) * D].mean(axis=0), rtol=0, atol=1e-14)
+    # one selected token: its value row
+    valid = np.array([0, 0, 1, 0, 0], np.int32)
+    o = oracle.attention(rng.standard_normal((4, D)), K, V, N, valid)
+    for j in range(4):
+        assert np.array_equal(o[j], V[2, (j // 2) * D:(j // 2 + 1) * D])
+    # two tokens, scores a/sqrt(D) and 0: weights e^s / (e^s + 1)
+    a = 3.0
+    K2 = np.zeros((2, N * D))
+    K2[0, 0] = 1.0
+    q = np.zeros((4, D))
+    q[0, 0] = a
+    o = oracle.attention(q, K2, V[:2], N)
+    s = a / math.sqrt(D)
+    want = (math.exp(s) * V[0, :D] + V[1, :D]) / (math.exp(s) + 1.0)
+    assert np.allclose(o[0], want, rtol=0, atol=1e-14)
+
+
+def test_attention_matches_scipy_softmax_with_grouped_heads_and_padding():
+    from scipy.special import softmax
+    rng = np.random.default_rng(10)
+    H, N, D, n = 8, 2, 16, 11
+    q = rng.standard_normal((H, D))
+    K = rng.standard_normal((n, N * D))
+    V = rng.standard_normal((n, N * D))
+    valid = (rng.uniform(size=n) > 0.3).astype(np.int32)
+    valid[0] = 1
+    o = oracle.attention(q, K, V, N, valid)
+    sel = np.nonzero(valid)[0]
+    for j in range(H):
+        h = j // (H // N)
+        s = K[sel, h * D:(h + 1) * D] @ q[j] / math.sqrt(D)
+        want = softmax(s) @ V[sel, h * D:(h + 1) * D]
+        assert np.allclose(o[j], want, rtol=1e-12, atol=1e-14)
+    # padding rows do not matter
+    K[valid == 0] += 100.0
+    V[valid == 0] -= 50.0
+    assert np.array_equal(oracle.attention(q, K, V, N, valid), o)
