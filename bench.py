@@ -311,6 +311,29 @@ def read_path(dev, steps=256, reps=3):
     r_flops = 2.0 * r_tok * cfg.d_c * cfg.W
     r_bytes = r_tok * restore_bytes_per_token(cfg) + bufs.n_ref * cfg.W * 1
     _, tf_burst, tf_sust, _ = _peaks()
+    # sparse attention of the same steps over the restored K^, V^ (32 query heads)
+    qs = [torch.from_numpy(wl.decode_queries(cfg, 0, st_).view(np.int16)).view(torch.bfloat16).to(dev)
+          for st_ in range(r_steps)]
+    ao = torch.empty((1, cfg.H, cfg.D), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(side):
+        bufs.attend(cfg.H, qs[0], ok_, ov_, sels[0].view(1, -1), ao, stream=side)
+    side.synchronize()
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=side):
+        for st_ in range(r_steps):
+            bufs.attend(cfg.H, qs[st_], ok_, ov_, sels[st_].view(1, -1), ao, stream=side)
+    ga.replay()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(reps):
+        ga.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    a_ms = a.elapsed_time(b) / (reps * r_steps)
+    a_bytes = r_tok * (2 * dk * 2 + 4) + cfg.H * cfg.D * (2 + 4)
+    attention = {"ms_per_step": a_ms, "steps": r_steps, "query_heads": cfg.H,
+                 "bytes_per_step": a_bytes, "achieved_gbs": a_bytes / (a_ms / 1e3) / 1e9,
+                 "frac_of_hbm": a_bytes / (a_ms / 1e3) / 1e9 / _peaks()[0]}
     restore = {"tokens_per_s": r_tok / (r_ms / 1e3), "ms_per_step": r_ms, "steps": r_steps,
                "flops_per_step": r_flops, "achieved_tflops": r_flops / (r_ms / 1e3) / 1e12,
                "frac_of_sustained": r_flops / (r_ms / 1e3) / 1e12 / tf_sust,
@@ -329,7 +352,7 @@ def read_path(dev, steps=256, reps=3):
             "unit": "GB/s", "frac": gbs / hbm, "peak_source": "%s HBM copy bandwidth" % src,
             "device_status": st,
             "compress_tokens_per_s": cfg.T / (c_ms / 1e3), "compress_ms": c_ms,
-            "compress_kernels_ms": c_prof, "restore": restore}
+            "compress_kernels_ms": c_prof, "restore": restore, "attention": attention}
 
 
 def run_ours(args, cfg):

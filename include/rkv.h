@@ -177,6 +177,21 @@ rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const r
                           const void *Wd, const int32_t *sel, int32_t n_sel, double rope_base,
                           void *out_k, void *out_v, int32_t *dev_status, void *stream);
 
+/* Sparse attention of one decode step over the restored set [RKV §2.7 = Sec. IV-C]:
+ *   out[lb][j] = softmax( q[lb][j] K^_I^T / sqrt(D) ) V^_I   for each query head j < H,
+ * query head j reading key/value head floor(j / (H/N)) (grouped heads; the page writes
+ * the formula per head).  I = the rows n < n_sel of k_hat/v_hat whose sel[lb][n] is a
+ * position in [0, T) (padding and out-of-range entries, zero rows of rkv_restore_kv,
+ * are left out); an empty I gives zeros.  Scores, softmax and sums in fp32.
+ * q: bf16 [L*B][H][D]; k_hat, v_hat: bf16 [L*B][n_sel][N D] (rkv_restore_kv's
+ * outputs); sel: as given to rkv_restore_kv; out: fp32 [L*B][H][D].
+ * workspace: >= the bytes rkv_attention_workspace reports (per-split partials).
+ * Requires kv_dtype bf16, D in {64, 128, 256}, H a multiple of N with H/N <= 8.     */
+rkv_status rkv_attention_workspace(const rkv_params *p, int32_t H, int32_t n_sel, size_t *bytes);
+rkv_status rkv_sparse_attention(const rkv_params *p, int32_t H, const void *q, const void *k_hat,
+                                const void *v_hat, const int32_t *sel, int32_t n_sel, float *out,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
 /* rkv_compress without a workspace argument: for callers that cannot allocate
  * device memory at the call site -- code running while a CUDA graph is captured
  * (cudaMalloc is not allowed there), runtimes whose device memory belongs to an

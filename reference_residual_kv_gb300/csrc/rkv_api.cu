@@ -271,4 +271,45 @@ rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const r
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
+static rkv_status check_attention(const rkv_params *p, int32_t H, int32_t n_sel)
+{
+    rkv_status st = check_params(p);
+    if (st != RKV_OK) return st;
+    if (n_sel < 0 || H <= 0) return RKV_ERR_INVALID_ARG;
+    if (p->kv_dtype != RKV_BF16) return RKV_ERR_UNSUPPORTED;
+    if ((p->D != 64 && p->D != 128 && p->D != 256) || H % p->N != 0 || H / p->N > 8)
+        return RKV_ERR_UNSUPPORTED;
+    return RKV_OK;
+}
+
+rkv_status rkv_attention_workspace(const rkv_params *p, int32_t H, int32_t n_sel, size_t *bytes)
+{
+    rkv_status st = check_attention(p, H, n_sel);
+    if (st != RKV_OK) return st;
+    if (!bytes) return RKV_ERR_INVALID_ARG;
+    *bytes = attention_workspace_bytes(make_geometry(p), H, n_sel);
+    return RKV_OK;
+}
+
+rkv_status rkv_sparse_attention(const rkv_params *p, int32_t H, const void *q, const void *k_hat,
+                                const void *v_hat, const int32_t *sel, int32_t n_sel, float *out,
+                                void *workspace, size_t workspace_bytes, void *stream)
+{
+    rkv_status st = check_attention(p, H, n_sel);
+    if (st != RKV_OK) return st;
+    Geometry g = make_geometry(p);
+    if (!q || !out) return RKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out)) return RKV_ERR_ALIGNMENT;
+    if (n_sel == 0) {
+        cudaError_t e = cudaMemsetAsync(out, 0, (size_t)g.LB * H * g.D * sizeof(float), (cudaStream_t)stream);
+        return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+    }
+    if (!k_hat || !v_hat || !sel) return RKV_ERR_INVALID_ARG;
+    if (!aligned16(k_hat) || !aligned16(v_hat) || !aligned16(sel)) return RKV_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < attention_workspace_bytes(g, H, n_sel)) return RKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RKV_ERR_ALIGNMENT;
+    cudaError_t e = launch_attention(g, H, q, k_hat, v_hat, sel, n_sel, out, workspace, (cudaStream_t)stream);
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -1,0 +1,199 @@
+// rkv_attention.cu -- sparse attention of one decode step over the restored set
+// [RKV §2.7 = Sec. IV-C]:
+//   o_j = softmax( q_j K^_I^T / sqrt(D) ) V^_I   for each query head j,
+// query head j reading key/value head floor(j / (H/N)); I = the selected rows that
+// are not padding.  Reading the restored K^ and V^ dominates (2 N D bf16 per token),
+// so the pass is bound by HBM and runs on CUDA cores in fp32:
+//   k_attn_split    one CTA per (split of the selected rows, KV head, layer-sequence):
+//                   each warp keeps an online softmax (running max, sum and weighted
+//                   value sum) per query head of the group over its rows, one row at a
+//                   time with D/32 coordinates per lane; the 8 warps merge in shared
+//                   memory and write the split's partial (max, sum, D sums).
+//   k_attn_combine  one warp per (layer-sequence, query head): merges the splits.
+#include "rkv_internal.cuh"
+
+#include <math.h>
+
+namespace rkv {
+namespace {
+
+constexpr int kMaxG = 8;          // query heads per key/value head
+constexpr int kWarps = 8;
+
+template <int EPL>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[EPL])
+{
+    if constexpr (EPL == 8) {
+        const uint4 u = __ldg((const uint4 *)p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[2 * j] = __uint_as_float(w[j] << 16);
+            x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        }
+    } else if constexpr (EPL == 4) {
+        const uint2 u = __ldg((const uint2 *)p);
+        x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+        x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+        const uint32_t u = __ldg((const uint32_t *)p);
+        x[0] = __uint_as_float(u << 16); x[1] = __uint_as_float(u & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Partials: [LB][N][splits][G][D + 2] floats = {D weighted sums, max, sum}.
+template <int EPL>
+__global__ void __launch_bounds__(32 * kWarps)
+k_attn_split(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kh,
+             const __nv_bfloat16 *__restrict__ vh, const int32_t *__restrict__ sel, int n_sel,
+             int T, int H, int N, int chunk, int splits, float scale, float *__restrict__ part)
+{
+    constexpr int D = 32 * EPL;
+    __shared__ float sm[kWarps][kMaxG][D + 2];
+    const int s = blockIdx.x, n = blockIdx.y, lb = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = H / N;
+    float qr[kMaxG][EPL], o[kMaxG][EPL], m[kMaxG], l[kMaxG];
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) { o[g][e] = 0.0f; qr[g][e] = 0.0f; }
+        if (g < G) {
+            load_row<EPL>(q + ((size_t)lb * H + n * G + g) * D + lane * EPL, qr[g]);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qr[g][e] *= scale;     // 1/sqrt(D), a power of 2 for D = 64, 256
+        }
+    }
+    const int r0 = s * chunk, r1 = min(n_sel, r0 + chunk);
+    const size_t rs = (size_t)N * D;                          // row stride of K^, V^
+    for (int r = r0 + warp; r < r1; r += kWarps) {
+        const int t = __ldg(sel + (size_t)lb * n_sel + r);
+        if (t < 0 || t >= T) continue;                        // padding (uniform per warp)
+        float kx[EPL], vx[EPL];
+        const size_t off = ((size_t)lb * n_sel + r) * rs + (size_t)n * D + lane * EPL;
+        load_row<EPL>(kh + off, kx);
+        load_row<EPL>(vh + off, vx);
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) {
+            if (g >= G) break;
+            float d = 0.0f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) d = fmaf(qr[g][e], kx[e], d);
+            const float sc = warp_sum(d);
+            const float mn = fmaxf(m[g], sc);
+            const float a = __expf(m[g] - mn), b = __expf(sc - mn);
+            l[g] = fmaf(l[g], a, b);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(o[g][e], a, b * vx[e]);
+            m[g] = mn;
+        }
+    }
+    // merge the warps
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g) {
+        if (g >= G) break;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) sm[warp][g][lane * EPL + e] = o[g][e];
+        if (lane == 0) { sm[warp][g][D] = m[g]; sm[warp][g][D + 1] = l[g]; }
+    }
+    __syncthreads();
+    for (int g = warp; g < G; g += kWarps) {
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm[w][g][D]);
+        float L = 0.0f, acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = M == -INFINITY ? 0.0f : __expf(sm[w][g][D] - M);
+            L = fmaf(sm[w][g][D + 1], f, L);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(sm[w][g][lane * EPL + e], f, acc[e]);
+        }
+        float *dst = part + ((((size_t)lb * N + n) * splits + s) * G + g) * (D + 2);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = acc[e];
+        if (lane == 0) { dst[D] = M; dst[D + 1] = L; }
+    }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+k_attn_combine(const float *__restrict__ part, int LB, int H, int N, int splits, float *__restrict__ out)
+{
+    constexpr int D = 32 * EPL;
+    const int lane = threadIdx.x & 31;
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (w >= (long long)LB * H) return;
+    const int lb = (int)(w / H), j = (int)(w % H);
+    const int G = H / N, n = j / G, g = j % G;
+    const float *base = part + (((size_t)lb * N + n) * splits) * G * (D + 2) + (size_t)g * (D + 2);
+    const size_t ss = (size_t)G * (D + 2);                   // split stride
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, base[s * ss + D]);
+    float L = 0.0f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+    for (int s = 0; s < splits; ++s) {
+        const float f = M == -INFINITY ? 0.0f : __expf(base[s * ss + D] - M);
+        L = fmaf(base[s * ss + D + 1], f, L);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(base[s * ss + lane * EPL + e], f, acc[e]);
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    float *dst = out + ((size_t)lb * H + j) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = acc[e] * inv;
+}
+
+constexpr int kChunk = 512;       // selected rows per split
+
+template <int EPL>
+cudaError_t run_attn(const Geometry &g, int H, const void *q, const void *kh, const void *vh,
+                     const int32_t *sel, int n_sel, float *out, float *part, cudaStream_t s)
+{
+    const int splits = (n_sel + kChunk - 1) / kChunk;
+    const float scale = (float)(1.0 / sqrt((double)g.D));
+    {
+        ProfScope prof("attention_split", s);
+        k_attn_split<EPL><<<dim3(splits, g.N, g.LB), 32 * kWarps, 0, s>>>(
+            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kh, (const __nv_bfloat16 *)vh, sel, n_sel,
+            g.T, H, g.N, kChunk, splits, scale, part);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    ProfScope prof("attention_combine", s);
+    const long long warps = (long long)g.LB * H;
+    k_attn_combine<EPL><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(part, g.LB, H, g.N, splits, out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_workspace_bytes(const Geometry &g, int H, int n_sel)
+{
+    const size_t splits = (size_t)((n_sel + kChunk - 1) / kChunk);
+    return (size_t)g.LB * H * splits * (g.D + 2) * sizeof(float);
+}
+
+cudaError_t launch_attention(const Geometry &g, int H, const void *q, const void *kh, const void *vh,
+                             const int32_t *sel, int n_sel, float *out, void *workspace, cudaStream_t s)
+{
+    float *part = (float *)workspace;
+    switch (g.D) {
+    case 64: return run_attn<2>(g, H, q, kh, vh, sel, n_sel, out, part, s);
+    case 128: return run_attn<4>(g, H, q, kh, vh, sel, n_sel, out, part, s);
+    case 256: return run_attn<8>(g, H, q, kh, vh, sel, n_sel, out, part, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rkv

@@ -101,6 +101,11 @@ int device_sm_count();
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
               uint64_t batch, uint32_t box_rows);
 
+// sparse attention over the restored set (rkv_attention.cu)
+size_t attention_workspace_bytes(const Geometry &g, int H, int n_sel);
+cudaError_t launch_attention(const Geometry &g, int H, const void *q, const void *kh, const void *vh,
+                             const int32_t *sel, int n_sel, float *out, void *workspace, cudaStream_t s);
+
 // restore of K and V for selected tokens (rkv_restore.cu)
 cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rkv_cache *cache,
                            const void *Wd, const int32_t *sel, int n_sel, double rope_base,

@@ -17,7 +17,7 @@ RKV_F32, RKV_BF16, RKV_FP8_E4M3 = 0, 1, 2
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_ALIGNMENT = 0, 1, 2, 3
 RKV_ERR_CUDA, RKV_ERR_INDEX, RKV_ERR_DEVICE_TIMEOUT, RKV_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("rkv_n_ref", "rkv_query_sizes", "rkv_build_ref_pool", "rkv_compress",
-            "rkv_gather_dequant", "rkv_restore_kv", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
+            "rkv_gather_dequant", "rkv_restore_kv", "rkv_attention_workspace", "rkv_sparse_attention", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
             "rkv_status_string")
 _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 
@@ -76,6 +76,10 @@ def lib():
         L.rkv_restore_kv.argtypes = [P, ctypes.POINTER(rkv_ref_pool), ctypes.POINTER(rkv_cache),
                                      V, V, I32, ctypes.c_double, V, V, V, V]
         L.rkv_restore_kv.restype = I32
+        L.rkv_attention_workspace.argtypes = [P, I32, I32, sz]
+        L.rkv_attention_workspace.restype = I32
+        L.rkv_sparse_attention.argtypes = [P, I32, V, V, V, V, I32, V, V, ctypes.c_size_t, V]
+        L.rkv_sparse_attention.restype = I32
         L.rkv_profile_enable.argtypes = [I32]
         L.rkv_profile_enable.restype = I32
         L.rkv_profile_collect.argtypes = [ctypes.c_char_p, I32, ctypes.POINTER(ctypes.c_float),
@@ -179,6 +183,23 @@ def rkv_restore_kv(p: rkv_params, pool: rkv_ref_pool, cache: rkv_cache, Wd, sel,
         raise RkvError(st, "rkv_restore_kv")
 
 
+def rkv_attention_workspace(p: rkv_params, H: int, n_sel: int) -> int:
+    b = ctypes.c_size_t()
+    st = lib().rkv_attention_workspace(ctypes.byref(p), int(H), int(n_sel), ctypes.byref(b))
+    if st:
+        raise RkvError(st, "rkv_attention_workspace")
+    return b.value
+
+
+def rkv_sparse_attention(p: rkv_params, H: int, q, k_hat, v_hat, sel, n_sel: int, out, workspace,
+                         workspace_bytes: int, stream=None) -> None:
+    st = lib().rkv_sparse_attention(ctypes.byref(p), int(H), _ptr(q), _ptr(k_hat), _ptr(v_hat),
+                                    _ptr(sel), int(n_sel), _ptr(out), _ptr(workspace),
+                                    int(workspace_bytes), _stream(stream))
+    if st:
+        raise RkvError(st, "rkv_sparse_attention")
+
+
 def rkv_profile_enable(on: bool) -> None:
     lib().rkv_profile_enable(1 if on else 0)
 
@@ -248,6 +269,14 @@ class Buffers:
     def restore(self, Wd, sel, out_k, out_v, rope_base: float, stream=None):
         rkv_restore_kv(self.p, self.pool, self.cache, Wd, sel, sel.shape[-1], rope_base, out_k,
                        out_v, self.status, stream)
+
+    def attend(self, H: int, q, k_hat, v_hat, sel, out, stream=None):
+        n_sel = sel.shape[-1]
+        need = rkv_attention_workspace(self.p, H, n_sel)
+        if getattr(self, "_attn_ws", None) is None or self._attn_ws.numel() < need:
+            self._attn_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.status.device)
+        rkv_sparse_attention(self.p, H, q, k_hat, v_hat, sel, n_sel, out, self._attn_ws,
+                             self._attn_ws.numel(), stream)
 
     def device_status(self) -> int:
         return int(self.status[0].item())

@@ -141,6 +141,7 @@ class Config:
     gather_tail: int = 512
     gather_steps: int = 0
     rope_base: float = 10000.0  # base of the rotary embedding applied to restored keys
+    H: int = 32                 # query heads of the attention that reads the cache
 
     @property
     def W(self) -> int:
@@ -158,7 +159,7 @@ CONFIGS = {
     "llama3.1-8b-kv": Config("llama3.1-8b-kv", seed=1, L=32, B=1, T=8192, N=8, D=128,
                              d_ff=1024, d_c=512, stride=8),
     "qwen2.5-7b-kv": Config("qwen2.5-7b-kv", seed=2, L=28, B=1, T=32768, N=4, D=128,
-                            d_ff=512, d_c=256, stride=8),
+                            d_ff=512, d_c=256, stride=8, H=28),
     "long-131k-fp8ref": Config("long-131k-fp8ref", seed=3, L=1, B=1, T=131072, N=8, D=128,
                                d_ff=1024, d_c=512, stride=16, ref_dtype="fp8", gather_steps=256),
     "multimodal-8x4096-int2": Config("multimodal-8x4096-int2", seed=4, L=1, B=8, T=4096, N=8,
@@ -275,6 +276,13 @@ def decoder_weights(cfg: Config, layer: int):
     (Wd[c][j] = W_d[j][c]), entries ~ N(0, 1/d_c)."""
     w = normal(stream_key(cfg.seed, TAG_WD, layer), cfg.W * cfg.d_c).reshape(cfg.W, cfg.d_c)
     return store(w * math.sqrt(1.0 / cfg.d_c), cfg.kv_dtype)
+
+
+def decode_queries(cfg: Config, layer: int, step: int) -> np.ndarray:
+    """Query vectors of one decode step of one layer, [B][H][D] ~ N(0, 1), stored in the
+    kv dtype (the model that would produce them is not part of this workload)."""
+    q = normal(stream_key(cfg.seed, TAG_QUERY, layer, step), cfg.B * cfg.H * cfg.D)
+    return store(q.reshape(cfg.B, cfg.H, cfg.D), cfg.kv_dtype)
 
 
 def synthetic_records(cfg: Config, n_ref: int, lb: int = 0):
