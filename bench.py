@@ -355,6 +355,45 @@ def read_path(dev, steps=256, reps=3):
             "compress_kernels_ms": c_prof, "restore": restore, "attention": attention}
 
 
+def decode_write(cfg, bufs, kv_d, W1, W2, W3, dev, calls=20, reps=3):
+    """The write side of one decode step: the token at the last position of every layer
+    appended with rkv_append_token (one call for all layers), `calls` calls in one CUDA
+    graph.  Bytes per call: W_c1, W_c2, W_c3 of every layer and the pool rows the exact
+    distances read; inputs device-resident."""
+    import torch
+    LB, t = cfg.L * cfg.B, cfg.T - 1
+    x = kv_d.view(LB, cfg.T, -1)[:, t].contiguous()
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        bufs.append(x, t, W1, W2, W3, stream=side)
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(calls):
+            bufs.append(x, t, W1, W2, W3, stream=side)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / (reps * calls)
+    pool = int(bufs.pool_size[t].item())
+    w_bytes = cfg.L * (2 * cfg.d_ff * cfg.W + cfg.d_c * cfg.d_ff) * 2
+    p_bytes = LB * pool * cfg.W * (1 if cfg.ref_dtype == "fp8" else 2)
+    hbm = _peaks()[0]
+    by = w_bytes + p_bytes
+    return {"workload": "%s: token %d of each of the %d layer-sequences appended in one call "
+                        "(pool of %d references)" % (cfg.name, t, LB, pool),
+            "ms_per_call": ms, "tokens_per_s": LB / (ms / 1e3), "bytes_per_call": by,
+            "achieved_gbs": by / (ms / 1e3) / 1e9, "frac_of_hbm": by / (ms / 1e3) / 1e9 / hbm,
+            "device_status": bufs.device_status()}
+
+
 def run_ours(args, cfg):
     import torch
     rank, ws, local = _dist_env()
@@ -513,6 +552,7 @@ def run_ours(args, cfg):
         "e2e": e2e,
     }
     if not args.no_read_path:
+        line["decode_write"] = decode_write(cfg, bufs, kv_d, W1, W2, W3, dev)
         del kv_d, G, W1, W2, W3, bufs, out_z, out_m
         torch.cuda.empty_cache()
         line["read_path"] = read_path(dev)

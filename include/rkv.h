@@ -192,6 +192,23 @@ rkv_status rkv_sparse_attention(const rkv_params *p, int32_t H, const void *q, c
                                 const void *v_hat, const int32_t *sel, int32_t n_sel, float *out,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* Decode-time write of one new token per (layer, sequence) [RKV §2.7 = Sec. IV-C,
+ * step 4 of a decode step]: the token at position t (the same t for every sequence)
+ * joins the cache.  At a reference position of the schedule its row is stored in the
+ * pool (copy or FP8 encode, squared norm) and its record is the reference record;
+ * otherwise it is encoded like rkv_compress encodes it: the k_t nearest references
+ * with pos < t by exact squared distance (ties to the lower slot), their mean in KV
+ * space, z = f_c(kv) - f_c(mean) (fp32 on CUDA cores), group quantisation.
+ * p->T is the capacity (0 <= t < T); tokens 0..t-1 must already be written (by
+ * rkv_compress, or by earlier calls) into `pool` and `cache`, whose schedule
+ * (rkv_build_ref_pool for capacity T) is fixed in advance.
+ * kv_new: [L*B][W] in kv_dtype; weights as for rkv_compress.
+ * workspace: >= workspace_bytes of rkv_query_sizes, 256-byte aligned.               */
+rkv_status rkv_append_token(const rkv_params *p, const void *kv_new, int32_t t,
+                            const rkv_ref_pool *pool, const void *W1t, const void *W2t,
+                            const void *W3t, const rkv_cache *cache, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream);
+
 /* rkv_compress without a workspace argument: for callers that cannot allocate
  * device memory at the call site -- code running while a CUDA graph is captured
  * (cudaMalloc is not allowed there), runtimes whose device memory belongs to an

@@ -271,6 +271,28 @@ rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const r
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
+rkv_status rkv_append_token(const rkv_params *p, const void *kv_new, int32_t t,
+                            const rkv_ref_pool *pool, const void *W1t, const void *W2t,
+                            const void *W3t, const rkv_cache *cache, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    rkv_status st = check_params(p);
+    if (st != RKV_OK) return st;
+    if (t < 0 || t >= p->T) return RKV_ERR_INVALID_ARG;
+    Geometry g = make_geometry(p);
+    if ((st = check_pool(pool, g.n_ref)) != RKV_OK) return st;
+    if ((st = check_cache(cache)) != RKV_OK) return st;
+    if (!kv_new || !W1t || !W2t || !W3t || !dev_status) return RKV_ERR_INVALID_ARG;
+    if (!aligned16(kv_new) || !aligned16(W1t) || !aligned16(W2t) || !aligned16(W3t) ||
+        !aligned16(dev_status))
+        return RKV_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < append_workspace_bytes(g)) return RKV_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255) != 0) return RKV_ERR_ALIGNMENT;
+    cudaError_t e = launch_append(g, kv_new, t, pool, W1t, W2t, W3t, cache, workspace, dev_status,
+                                  (cudaStream_t)stream);
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
 static rkv_status check_attention(const rkv_params *p, int32_t H, int32_t n_sel)
 {
     rkv_status st = check_params(p);

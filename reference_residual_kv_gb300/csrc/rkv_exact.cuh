@@ -1,0 +1,106 @@
+// rkv_exact.cuh -- exact squared distances and small sorted lists, shared by the
+// top-k finalisation (rkv_topk.cu) and the single-token write (rkv_append.cu) so that
+// both rank references by the same fp32 values.
+//
+// Exact distances sum (x - r)^2 in fp32.  For bf16 tokens and bf16 or FP8 references
+// x - r is exact in fp32 (both operands decode exactly); each group of 8 squares is
+// added as a tree, a lane keeps four partial sums over its groups, and the warp adds
+// its lanes as a tree.
+#pragma once
+
+#include "rkv_internal.cuh"
+
+namespace rkv {
+
+template <typename T> struct Vec8;
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[8])
+    {
+        float4 a = *(const float4 *)p, b = *(const float4 *)(p + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8])
+    {
+        uint4 raw = *(const uint4 *)p;
+        const __nv_bfloat16 *h = (const __nv_bfloat16 *)&raw;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(h[j]);
+    }
+};
+template <> struct Vec8<uint8_t> {      // FP8 E4M3 bytes, decoded exactly
+    static __device__ __forceinline__ void load(const uint8_t *p, float (&v)[8])
+    {
+        const uint2 raw = *(const uint2 *)p;
+        const uint8_t *b = (const uint8_t *)&raw;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __nv_fp8_e4m3 q;
+            q.__x = b[j];
+            v[j] = (float)q;
+        }
+    }
+};
+
+__device__ __forceinline__ float warp_tree_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename TX, typename TR>
+__device__ __forceinline__ float sq8(const TX *x, const TR *r)
+{
+    float a[8], b[8], s[8];
+    Vec8<TX>::load(x, a);
+    Vec8<TR>::load(r, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float d = a[j] - b[j];
+        s[j] = d * d;
+    }
+    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
+// Exact squared distance of two rows, summed by the whole warp (four 8-element groups
+// of a lane in flight at once).
+template <typename TX, typename TR = TX>
+__device__ __forceinline__ float warp_sqdist(const TX *x, const TR *r, int W, int lane)
+{
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int c = lane * 8;
+    for (; c + 3 * 256 < W; c += 4 * 256) {
+        float p[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p[u] = sq8(x + c + u * 256, r + c + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] += p[u];
+    }
+    for (; c < W; c += 256) acc[0] += sq8(x + c, r + c);
+    return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+}
+
+__device__ __forceinline__ bool key_less(float ea, int sa, float eb, int sb)
+{
+    return ea < eb || (ea == eb && (unsigned)sa < (unsigned)sb);
+}
+
+// Insert (e, s) into an ascending list of n entries (registers, uniform per lane).
+template <int N>
+__device__ __forceinline__ void list_insert(float (&le)[N], int (&ls)[N], float e, int s)
+{
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        bool lt = key_less(e, s, le[q], ls[q]);
+        float te = lt ? le[q] : e;
+        int ts = lt ? ls[q] : s;
+        if (lt) { le[q] = e; ls[q] = s; }
+        e = te;
+        s = ts;
+    }
+}
+
+}  // namespace rkv

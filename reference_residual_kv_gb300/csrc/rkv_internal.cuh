@@ -101,6 +101,14 @@ int device_sm_count();
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
               uint64_t batch, uint32_t box_rows);
 
+// single-token write (rkv_pool.cu: the pool entry; rkv_append.cu: the record)
+cudaError_t launch_append_ref(const Geometry &g, const void *kv_new, int t, const rkv_ref_pool *pool,
+                              cudaStream_t s);
+size_t append_workspace_bytes(const Geometry &g);
+cudaError_t launch_append(const Geometry &g, const void *kv_new, int t, const rkv_ref_pool *pool,
+                          const void *W1t, const void *W2t, const void *W3t, const rkv_cache *cache,
+                          void *ws, int32_t *status, cudaStream_t s);
+
 // sparse attention over the restored set (rkv_attention.cu)
 size_t attention_workspace_bytes(const Geometry &g, int H, int n_sel);
 cudaError_t launch_attention(const Geometry &g, int H, const void *q, const void *kh, const void *vh,

@@ -26,21 +26,16 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// One warp per (lb, reference slot): copy (or FP8-encode) the token's row and take
-// the squared norm of the stored values in fp32.
+// One warp stores one reference row: copy (or FP8-encode) the token's row into pool row
+// `row` and take the squared norm of the stored values in fp32.
 template <typename TIn, int OUT_FP8>
-__global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restrict__ ref_pos,
-                             void *ref_vec, float *__restrict__ ref_sqnorm, int LB, int T, int W,
-                             int n_ref)
+__device__ __forceinline__ void store_ref_row(const TIn *__restrict__ src, void *ref_vec,
+                                              float *__restrict__ ref_sqnorm, size_t row, int W,
+                                              int lane)
 {
-    const int lane = threadIdx.x & 31;
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (gw >= (long long)LB * n_ref) return;
-    const int lb = (int)(gw / n_ref), m = (int)(gw % n_ref);
-    const TIn *src = kv + ((size_t)lb * T + ref_pos[m]) * W;
     float acc = 0.0f;
     if constexpr (sizeof(TIn) == 4) {
-        float *dst = (float *)ref_vec + ((size_t)lb * n_ref + m) * W;
+        float *dst = (float *)ref_vec + row * W;
         for (int c = lane * 4; c < W; c += 128) {
             float4 v = *(const float4 *)(src + c);
             *(float4 *)(dst + c) = v;
@@ -62,10 +57,10 @@ __global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restri
                     q.__x = b[j];
                     f[j] = (float)q;
                 }
-                uint8_t *dst = (uint8_t *)ref_vec + ((size_t)lb * n_ref + m) * W;
+                uint8_t *dst = (uint8_t *)ref_vec + row * W;
                 *(uint2 *)(dst + c) = *(const uint2 *)b;
             } else {
-                __nv_bfloat16 *dst = (__nv_bfloat16 *)ref_vec + ((size_t)lb * n_ref + m) * W;
+                __nv_bfloat16 *dst = (__nv_bfloat16 *)ref_vec + row * W;
                 *(uint4 *)(dst + c) = raw;
             }
             float s = 0.0f;
@@ -75,7 +70,54 @@ __global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restri
         }
     }
     acc = warp_sum(acc);
-    if (lane == 0) ref_sqnorm[(size_t)lb * n_ref + m] = acc;
+    if (lane == 0) ref_sqnorm[row] = acc;
+}
+
+// One warp per (lb, reference slot).
+template <typename TIn, int OUT_FP8>
+__global__ void k_build_refs(const TIn *__restrict__ kv, const int32_t *__restrict__ ref_pos,
+                             void *ref_vec, float *__restrict__ ref_sqnorm, int LB, int T, int W,
+                             int n_ref)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= (long long)LB * n_ref) return;
+    const int lb = (int)(gw / n_ref), m = (int)(gw % n_ref);
+    store_ref_row<TIn, OUT_FP8>(kv + ((size_t)lb * T + ref_pos[m]) * W, ref_vec, ref_sqnorm,
+                                (size_t)lb * n_ref + m, W, lane);
+}
+
+// Single-token write: one warp per lb stores the new token's row if position t is a
+// reference position (the schedule is the same for every sequence).
+template <typename TIn, int OUT_FP8>
+__global__ void k_append_ref(const TIn *__restrict__ kv_new, int t, const int32_t *__restrict__ ref_slot,
+                             void *ref_vec, float *__restrict__ ref_sqnorm, int LB, int W, int n_ref)
+{
+    const int lane = threadIdx.x & 31;
+    const int lb = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (lb >= LB) return;
+    const int slot = ref_slot[t];
+    if (slot < 0) return;
+    store_ref_row<TIn, OUT_FP8>(kv_new + (size_t)lb * W, ref_vec, ref_sqnorm, (size_t)lb * n_ref + slot,
+                                W, lane);
+}
+
+cudaError_t launch_append_ref(const Geometry &g, const void *kv_new, int t, const rkv_ref_pool *pool,
+                              cudaStream_t s)
+{
+    if (g.n_ref == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((g.LB * 32 + 255) / 256);
+    ProfScope prof("append_ref", s);
+    if (g.kv_dtype == RKV_F32)
+        k_append_ref<float, 0><<<blocks, 256, 0, s>>>((const float *)kv_new, t, pool->ref_slot,
+                                                      pool->ref_vec, pool->ref_sqnorm, g.LB, g.W, g.n_ref);
+    else if (g.ref_dtype == RKV_FP8_E4M3)
+        k_append_ref<__nv_bfloat16, 1><<<blocks, 256, 0, s>>>((const __nv_bfloat16 *)kv_new, t, pool->ref_slot,
+                                                              pool->ref_vec, pool->ref_sqnorm, g.LB, g.W, g.n_ref);
+    else
+        k_append_ref<__nv_bfloat16, 0><<<blocks, 256, 0, s>>>((const __nv_bfloat16 *)kv_new, t, pool->ref_slot,
+                                                              pool->ref_vec, pool->ref_sqnorm, g.LB, g.W, g.n_ref);
+    return cudaGetLastError();
 }
 
 // Dynamic stride: the positions follow a recurrence, so one thread writes them in

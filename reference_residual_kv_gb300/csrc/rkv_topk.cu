@@ -25,67 +25,9 @@
 // eight warps in parallel (near-tied clusters of FP8-rounded references otherwise
 // leave single warps scanning thousands of references one after another).
 #include "rkv_internal.cuh"
+#include "rkv_exact.cuh"
 
 namespace rkv {
-
-template <typename T> struct Vec8;
-template <> struct Vec8<float> {
-    static __device__ __forceinline__ void load(const float *p, float (&v)[8])
-    {
-        float4 a = *(const float4 *)p, b = *(const float4 *)(p + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-};
-template <> struct Vec8<__nv_bfloat16> {
-    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8])
-    {
-        uint4 raw = *(const uint4 *)p;
-        const __nv_bfloat16 *h = (const __nv_bfloat16 *)&raw;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(h[j]);
-    }
-};
-
-__device__ __forceinline__ float warp_tree_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-template <typename T>
-__device__ __forceinline__ float sq8(const T *x, const T *r)
-{
-    float a[8], b[8], s[8];
-    Vec8<T>::load(x, a);
-    Vec8<T>::load(r, b);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float d = a[j] - b[j];
-        s[j] = d * d;
-    }
-    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-}
-
-// Exact squared distance of two rows, summed by the whole warp: each lane's 8-element
-// groups are squared and added as trees, four groups of the lane in flight at once
-// (independent partial sums), and the lanes are added as a tree.
-template <typename T>
-__device__ __forceinline__ float warp_sqdist(const T *x, const T *r, int W, int lane)
-{
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int c = lane * 8;
-    for (; c + 3 * 256 < W; c += 4 * 256) {
-        float p[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) p[u] = sq8(x + c + u * 256, r + c + u * 256);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc[u] += p[u];
-    }
-    for (; c < W; c += 256) acc[0] += sq8(x + c, r + c);
-    return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-}
 
 template <typename T>
 __device__ __forceinline__ float warp_sqnorm(const T *x, int W, int lane)
@@ -109,26 +51,6 @@ __device__ __forceinline__ float warp_sqnorm(const T *x, int W, int lane)
         for (int j = 0; j < 8; ++j) acc[0] = fmaf(a[j], a[j], acc[0]);
     }
     return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-}
-
-__device__ __forceinline__ bool key_less(float ea, int sa, float eb, int sb)
-{
-    return ea < eb || (ea == eb && (unsigned)sa < (unsigned)sb);
-}
-
-// Insert (e, s) into an ascending list of n entries (registers, uniform per lane).
-template <int N>
-__device__ __forceinline__ void list_insert(float (&le)[N], int (&ls)[N], float e, int s)
-{
-#pragma unroll
-    for (int q = 0; q < N; ++q) {
-        bool lt = key_less(e, s, le[q], ls[q]);
-        float te = lt ? le[q] : e;
-        int ts = lt ? ls[q] : s;
-        if (lt) { le[q] = e; ls[q] = s; }
-        e = te;
-        s = ts;
-    }
 }
 
 constexpr int kNoSlot = 0x7fffffff;

@@ -17,7 +17,8 @@ RKV_F32, RKV_BF16, RKV_FP8_E4M3 = 0, 1, 2
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_ALIGNMENT = 0, 1, 2, 3
 RKV_ERR_CUDA, RKV_ERR_INDEX, RKV_ERR_DEVICE_TIMEOUT, RKV_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("rkv_n_ref", "rkv_query_sizes", "rkv_build_ref_pool", "rkv_compress",
-            "rkv_gather_dequant", "rkv_restore_kv", "rkv_attention_workspace", "rkv_sparse_attention", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
+            "rkv_gather_dequant", "rkv_restore_kv", "rkv_attention_workspace", "rkv_sparse_attention",
+            "rkv_append_token", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
             "rkv_status_string")
 _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 
@@ -76,6 +77,9 @@ def lib():
         L.rkv_restore_kv.argtypes = [P, ctypes.POINTER(rkv_ref_pool), ctypes.POINTER(rkv_cache),
                                      V, V, I32, ctypes.c_double, V, V, V, V]
         L.rkv_restore_kv.restype = I32
+        L.rkv_append_token.argtypes = [P, V, I32, ctypes.POINTER(rkv_ref_pool), V, V, V,
+                                       ctypes.POINTER(rkv_cache), V, ctypes.c_size_t, V, V]
+        L.rkv_append_token.restype = I32
         L.rkv_attention_workspace.argtypes = [P, I32, I32, sz]
         L.rkv_attention_workspace.restype = I32
         L.rkv_sparse_attention.argtypes = [P, I32, V, V, V, V, I32, V, V, ctypes.c_size_t, V]
@@ -183,6 +187,15 @@ def rkv_restore_kv(p: rkv_params, pool: rkv_ref_pool, cache: rkv_cache, Wd, sel,
         raise RkvError(st, "rkv_restore_kv")
 
 
+def rkv_append_token(p: rkv_params, kv_new, t: int, pool: rkv_ref_pool, W1t, W2t, W3t,
+                     cache: rkv_cache, workspace, workspace_bytes: int, dev_status, stream=None) -> None:
+    st = lib().rkv_append_token(ctypes.byref(p), _ptr(kv_new), int(t), ctypes.byref(pool), _ptr(W1t),
+                                _ptr(W2t), _ptr(W3t), ctypes.byref(cache), _ptr(workspace),
+                                int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    if st:
+        raise RkvError(st, "rkv_append_token")
+
+
 def rkv_attention_workspace(p: rkv_params, H: int, n_sel: int) -> int:
     b = ctypes.c_size_t()
     st = lib().rkv_attention_workspace(ctypes.byref(p), int(H), int(n_sel), ctypes.byref(b))
@@ -269,6 +282,10 @@ class Buffers:
     def restore(self, Wd, sel, out_k, out_v, rope_base: float, stream=None):
         rkv_restore_kv(self.p, self.pool, self.cache, Wd, sel, sel.shape[-1], rope_base, out_k,
                        out_v, self.status, stream)
+
+    def append(self, kv_new, t: int, W1t, W2t, W3t, stream=None):
+        rkv_append_token(self.p, kv_new, t, self.pool, W1t, W2t, W3t, self.cache, self.workspace,
+                         self.workspace_bytes, self.status, stream)
 
     def attend(self, H: int, q, k_hat, v_hat, sel, out, stream=None):
         n_sel = sel.shape[-1]
