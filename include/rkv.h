@@ -186,7 +186,8 @@ rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const r
  * q: bf16 [L*B][H][D]; k_hat, v_hat: bf16 [L*B][n_sel][N D] (rkv_restore_kv's
  * outputs); sel: as given to rkv_restore_kv; out: fp32 [L*B][H][D].
  * workspace: >= the bytes rkv_attention_workspace reports (per-split partials).
- * Requires kv_dtype bf16, D in {64, 128, 256}, H a multiple of N with H/N <= 8.     */
+ * Requires kv_dtype bf16, D in {64, 128, 256}, H a multiple of N with H/N <= 8
+ * (H/N <= 4 for D = 256).                                                          */
 rkv_status rkv_attention_workspace(const rkv_params *p, int32_t H, int32_t n_sel, size_t *bytes);
 rkv_status rkv_sparse_attention(const rkv_params *p, int32_t H, const void *q, const void *k_hat,
                                 const void *v_hat, const int32_t *sel, int32_t n_sel, float *out,

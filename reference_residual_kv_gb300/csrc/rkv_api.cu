@@ -299,7 +299,8 @@ static rkv_status check_attention(const rkv_params *p, int32_t H, int32_t n_sel)
     if (st != RKV_OK) return st;
     if (n_sel < 0 || H <= 0) return RKV_ERR_INVALID_ARG;
     if (p->kv_dtype != RKV_BF16) return RKV_ERR_UNSUPPORTED;
-    if ((p->D != 64 && p->D != 128 && p->D != 256) || H % p->N != 0 || H / p->N > 8)
+    if ((p->D != 64 && p->D != 128 && p->D != 256) || H % p->N != 0 || H / p->N > 8 ||
+        (p->D == 256 && H / p->N > 4))
         return RKV_ERR_UNSUPPORTED;
     return RKV_OK;
 }

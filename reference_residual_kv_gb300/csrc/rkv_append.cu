@@ -163,14 +163,6 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
     }
 }
 
-template <typename TX>
-__device__ __forceinline__ float xval(const TX *p);
-template <> __device__ __forceinline__ float xval<float>(const float *p) { return *p; }
-template <> __device__ __forceinline__ float xval<__nv_bfloat16>(const __nv_bfloat16 *p)
-{
-    return __bfloat162float(*p);
-}
-
 __device__ __forceinline__ float swish(float u) { return u / (1.0f + expf(-u)); }
 
 // One warp per d_ff column f: the four dot products of length W.
@@ -192,13 +184,20 @@ k_app_h(const TX *__restrict__ kv_new, const TX *__restrict__ W1t, const TX *__r
     const float *m = mean + (size_t)lb * W;
     const size_t wrow = ((size_t)(lb / B) * d_ff + f) * W;
     float a1 = 0.0f, a2 = 0.0f, b1 = 0.0f, b2 = 0.0f;
-    for (int c = lane; c < W; c += 32) {
-        const float w1 = xval(W1t + wrow + c), w2 = xval(W2t + wrow + c);
-        const float xv = xval(x + c), mv = m[c];
-        a1 = fmaf(xv, w1, a1);
-        a2 = fmaf(xv, w2, a2);
-        b1 = fmaf(mv, w1, b1);
-        b2 = fmaf(mv, w2, b2);
+    // 8 consecutive coordinates per lane and step (16-byte loads of bf16 rows)
+    for (int c = lane * 8; c < W; c += 256) {
+        float w1[8], w2[8], xv[8], mv[8];
+        Vec8<TX>::load(W1t + wrow + c, w1);
+        Vec8<TX>::load(W2t + wrow + c, w2);
+        Vec8<TX>::load(x + c, xv);
+        Vec8<float>::load(m + c, mv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            a1 = fmaf(xv[j], w1[j], a1);
+            a2 = fmaf(xv[j], w2[j], a2);
+            b1 = fmaf(mv[j], w1[j], b1);
+            b2 = fmaf(mv[j], w2[j], b2);
+        }
     }
     a1 = warp_tree_sum(a1);
     a2 = warp_tree_sum(a2);
@@ -219,7 +218,13 @@ k_app_z(const TX *__restrict__ W3t, int d_ff, int d_c, int B, const float *__res
     const float *h = dh + (size_t)lb * d_ff;
     const TX *w = W3t + ((size_t)(lb / B) * d_c + j) * d_ff;
     float acc = 0.0f;
-    for (int f = lane; f < d_ff; f += 32) acc = fmaf(h[f], xval(w + f), acc);
+    for (int f = lane * 8; f < d_ff; f += 256) {
+        float hv[8], wv[8];
+        Vec8<float>::load(h + f, hv);
+        Vec8<TX>::load(w + f, wv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc = fmaf(hv[j], wv[j], acc);
+    }
     acc = warp_tree_sum(acc);
     if (lane == 0) z[(size_t)lb * d_c + j] = acc;
 }

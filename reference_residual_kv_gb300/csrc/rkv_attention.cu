@@ -6,10 +6,10 @@
 // so the pass is bound by HBM and runs on CUDA cores in fp32:
 //   k_attn_split    one CTA per (split of the selected rows, KV head, layer-sequence):
 //                   each warp keeps an online softmax (running max, sum and weighted
-//                   value sum) per query head of the group over its rows, one row at a
-//                   time with D/32 coordinates per lane; the 8 warps merge in shared
+//                   value sum) per query head of the group over its rows, four rows'
+//                   loads at a time, D/32 coordinates per lane; the 8 warps merge in shared
 //                   memory and write the split's partial (max, sum, D sums).
-//   k_attn_combine  one warp per (layer-sequence, query head): merges the splits.
+//   k_attn_combine  one block per (layer-sequence, query head): merges the splits.
 #include "rkv_internal.cuh"
 
 #include <math.h>
@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kMaxG = 8;          // query heads per key/value head
 constexpr int kWarps = 8;
+constexpr int kRows = 4;          // rows a warp loads at once
 
 template <int EPL>
 __device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[EPL])
@@ -49,20 +50,20 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // Partials: [LB][N][splits][G][D + 2] floats = {D weighted sums, max, sum}.
-template <int EPL>
-__global__ void __launch_bounds__(32 * kWarps)
+template <int EPL, int GM>
+__global__ void __launch_bounds__(32 * kWarps, 2)
 k_attn_split(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kh,
              const __nv_bfloat16 *__restrict__ vh, const int32_t *__restrict__ sel, int n_sel,
              int T, int H, int N, int chunk, int splits, float scale, float *__restrict__ part)
 {
     constexpr int D = 32 * EPL;
-    __shared__ float sm[kWarps][kMaxG][D + 2];
+    __shared__ float sm[kWarps][GM][D + 2];
     const int s = blockIdx.x, n = blockIdx.y, lb = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = H / N;
-    float qr[kMaxG][EPL], o[kMaxG][EPL], m[kMaxG], l[kMaxG];
+    float qr[GM][EPL], o[GM][EPL], m[GM], l[GM];
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
+    for (int g = 0; g < GM; ++g) {
         m[g] = -INFINITY;
         l[g] = 0.0f;
 #pragma unroll
@@ -75,31 +76,45 @@ k_attn_split(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restric
     }
     const int r0 = s * chunk, r1 = min(n_sel, r0 + chunk);
     const size_t rs = (size_t)N * D;                          // row stride of K^, V^
-    for (int r = r0 + warp; r < r1; r += kWarps) {
-        const int t = __ldg(sel + (size_t)lb * n_sel + r);
-        if (t < 0 || t >= T) continue;                        // padding (uniform per warp)
-        float kx[EPL], vx[EPL];
-        const size_t off = ((size_t)lb * n_sel + r) * rs + (size_t)n * D + lane * EPL;
-        load_row<EPL>(kh + off, kx);
-        load_row<EPL>(vh + off, vx);
+    // kRows rows per warp and iteration: all their loads are issued before the first
+    // score is formed
+    for (int rb = r0 + warp * kRows; rb < r1; rb += kWarps * kRows) {
+        int t_l = -1;
+        if (lane < kRows && rb + lane < r1) t_l = __ldg(sel + (size_t)lb * n_sel + rb + lane);
+        float kx[kRows][EPL], vx[kRows][EPL];
+        bool ok[kRows];
 #pragma unroll
-        for (int g = 0; g < kMaxG; ++g) {
-            if (g >= G) break;
-            float d = 0.0f;
+        for (int u = 0; u < kRows; ++u) {
+            const int t = __shfl_sync(0xffffffffu, t_l, u);
+            ok[u] = t >= 0 && t < T;                          // padding: uniform per warp
+            if (ok[u]) {
+                const size_t off = ((size_t)lb * n_sel + rb + u) * rs + (size_t)n * D + lane * EPL;
+                load_row<EPL>(kh + off, kx[u]);
+                load_row<EPL>(vh + off, vx[u]);
+            }
+        }
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) d = fmaf(qr[g][e], kx[e], d);
-            const float sc = warp_sum(d);
-            const float mn = fmaxf(m[g], sc);
-            const float a = __expf(m[g] - mn), b = __expf(sc - mn);
-            l[g] = fmaf(l[g], a, b);
+        for (int u = 0; u < kRows; ++u) {
+            if (!ok[u]) continue;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(o[g][e], a, b * vx[e]);
-            m[g] = mn;
+            for (int g = 0; g < GM; ++g) {
+                if (g >= G) break;
+                float d = 0.0f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) d = fmaf(qr[g][e], kx[u][e], d);
+                const float sc = warp_sum(d);
+                const float mn = fmaxf(m[g], sc);
+                const float a = __expf(m[g] - mn), b = __expf(sc - mn);
+                l[g] = fmaf(l[g], a, b);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(o[g][e], a, b * vx[u][e]);
+                m[g] = mn;
+            }
         }
     }
     // merge the warps
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
+    for (int g = 0; g < GM; ++g) {
         if (g >= G) break;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) sm[warp][g][lane * EPL + e] = o[g][e];
@@ -125,36 +140,59 @@ k_attn_split(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restric
     }
 }
 
+// One block per (layer-sequence, query head): the maximum over the splits, then each
+// warp accumulates a strided subset of the splits, merged in shared memory.
 template <int EPL>
-__global__ void __launch_bounds__(256)
-k_attn_combine(const float *__restrict__ part, int LB, int H, int N, int splits, float *__restrict__ out)
+__global__ void __launch_bounds__(32 * kWarps)
+k_attn_combine(const float *__restrict__ part, int H, int N, int splits, float *__restrict__ out)
 {
     constexpr int D = 32 * EPL;
-    const int lane = threadIdx.x & 31;
-    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (w >= (long long)LB * H) return;
-    const int lb = (int)(w / H), j = (int)(w % H);
+    __shared__ float red[kWarps];
+    __shared__ float acc_s[kWarps][D + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lb = blockIdx.x / H, j = blockIdx.x % H;
     const int G = H / N, n = j / G, g = j % G;
     const float *base = part + (((size_t)lb * N + n) * splits) * G * (D + 2) + (size_t)g * (D + 2);
     const size_t ss = (size_t)G * (D + 2);                   // split stride
     float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, base[s * ss + D]);
+    for (int s = threadIdx.x; s < splits; s += blockDim.x) M = fmaxf(M, base[s * ss + D]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
     float L = 0.0f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-    for (int s = 0; s < splits; ++s) {
+    for (int s = warp; s < splits; s += kWarps) {
         const float f = M == -INFINITY ? 0.0f : __expf(base[s * ss + D] - M);
         L = fmaf(base[s * ss + D + 1], f, L);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] = fmaf(base[s * ss + lane * EPL + e], f, acc[e]);
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    float *dst = out + ((size_t)lb * H + j) * D + lane * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dst[e] = acc[e] * inv;
+    for (int e = 0; e < EPL; ++e) acc_s[warp][lane * EPL + e] = acc[e];
+    if (lane == 0) acc_s[warp][D] = L;
+    __syncthreads();
+    if (warp == 0) {
+        float Lt = 0.0f, a[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) a[e] = 0.0f;
+        for (int w = 0; w < kWarps; ++w) {
+            Lt += acc_s[w][D];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) a[e] += acc_s[w][lane * EPL + e];
+        }
+        const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+        float *dst = out + ((size_t)lb * H + j) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[e] = a[e] * inv;
+    }
 }
 
-constexpr int kChunk = 512;       // selected rows per split
+constexpr int kChunk = 256;       // selected rows per split
 
 template <int EPL>
 cudaError_t run_attn(const Geometry &g, int H, const void *q, const void *kh, const void *vh,
@@ -164,15 +202,21 @@ cudaError_t run_attn(const Geometry &g, int H, const void *q, const void *kh, co
     const float scale = (float)(1.0 / sqrt((double)g.D));
     {
         ProfScope prof("attention_split", s);
-        k_attn_split<EPL><<<dim3(splits, g.N, g.LB), 32 * kWarps, 0, s>>>(
-            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kh, (const __nv_bfloat16 *)vh, sel, n_sel,
-            g.T, H, g.N, kChunk, splits, scale, part);
+        if (H / g.N <= 4)
+            k_attn_split<EPL, 4><<<dim3(splits, g.N, g.LB), 32 * kWarps, 0, s>>>(
+                (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kh, (const __nv_bfloat16 *)vh, sel, n_sel,
+                g.T, H, g.N, kChunk, splits, scale, part);
+        else if constexpr (EPL < 8)
+            k_attn_split<EPL, kMaxG><<<dim3(splits, g.N, g.LB), 32 * kWarps, 0, s>>>(
+                (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kh, (const __nv_bfloat16 *)vh, sel, n_sel,
+                g.T, H, g.N, kChunk, splits, scale, part);
+        else
+            return cudaErrorInvalidValue;                     // D = 256 takes groups of <= 4
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     ProfScope prof("attention_combine", s);
-    const long long warps = (long long)g.LB * H;
-    k_attn_combine<EPL><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(part, g.LB, H, g.N, splits, out);
+    k_attn_combine<EPL><<<(unsigned)(g.LB * H), 32 * kWarps, 0, s>>>(part, H, g.N, splits, out);
     return cudaGetLastError();
 }
 
