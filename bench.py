@@ -58,6 +58,24 @@ def _dist_env():
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The largest value of x over the ranks (the job's time is its slowest rank's)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ms_local: float, units_per_rank: float, ws: int, device=None):
+    """(ms, units per second of the whole job): every rank processes units_per_rank in
+    its ms_local; the job's time is the slowest rank's."""
+    ms = max_over_ranks(ms_local, ws, device)
+    return ms, units_per_rank * ws / (ms / 1e3)
+
+
 def workload_description(cfg: wl.Config) -> dict:
     return {
         "workload": "%s: %d layers x %d seq x %d tokens, kv width %d (N=%d, D=%d), d_ff=%d, "
@@ -462,14 +480,8 @@ def run_ours(args, cfg):
     prof = rkv.rkv_profile_collect()
     rkv.rkv_profile_enable(False)
     barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     tokens_per_step = cfg.L * cfg.B * cfg.T
-    value = tokens_per_step * ws / (ms / 1e3)
+    ms, value = job_rate(e0.elapsed_time(e1) / args.steps, tokens_per_step, ws, dev)
 
     # ---- end to end: host buffers in, compressed cache and reads out
     e2e = None
@@ -497,13 +509,8 @@ def run_ours(args, cfg):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        ms_e2e = a.elapsed_time(b) / n_e2e
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": tokens_per_step * ws / (ms_e2e / 1e3), "unit": UNIT,
+        ms_e2e, v_e2e = job_rate(a.elapsed_time(b) / n_e2e, tokens_per_step, ws, dev)
+        e2e = {"value": v_e2e, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ms_e2e}
     if rank != 0:
