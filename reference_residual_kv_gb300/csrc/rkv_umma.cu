@@ -384,24 +384,34 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         float v[32];
                         um::tmem_ld32(tb + c0, v);
                         const float rn_l = (s0 + lane < a.n_ref) ? rn[s0 + lane] : 0.0f;
+                        // the columns whose expansion is below this row's current 8th
+                        // entry (a superset of those that will enter: the bound only falls)
+                        const float thr = be[kList - 1];
+                        uint32_t hit = 0u;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const float rj = __shfl_sync(0xffffffffu, rn_l, j);
-                            const float e = fmaf(-2.0f, v[j], rj);
-                            if (s0 + j < pool && e < be[kList - 1]) {
-                                // this warp's slots arrive in increasing order: strict <
-                                // keeps the lower slot ahead of an equal later one
-                                float ce = e;
-                                int cs = s0 + j;
+                            v[j] = fmaf(-2.0f, v[j], rj);
+                            hit |= (uint32_t)(s0 + j < pool && v[j] < thr) << j;
+                        }
+                        // each lane inserts only its own hits, in increasing column order
+                        // (strict < keeps the lower slot ahead of an equal later one), so
+                        // the warp runs the insertion max-popcount times, not once per
+                        // column some lane needs
+                        while (hit) {
+                            const int j = __ffs(hit) - 1;
+                            hit &= hit - 1u;
+                            float ce = v[j];
+                            if (!(ce < be[kList - 1])) continue;
+                            int cs = s0 + j;
 #pragma unroll
-                                for (int qq = 0; qq < kList; ++qq) {
-                                    const bool lt = ce < be[qq];
-                                    const float te = lt ? be[qq] : ce;
-                                    const int ts = lt ? bs[qq] : cs;
-                                    if (lt) { be[qq] = ce; bs[qq] = cs; }
-                                    ce = te;
-                                    cs = ts;
-                                }
+                            for (int qq = 0; qq < kList; ++qq) {
+                                const bool lt = ce < be[qq];
+                                const float te = lt ? be[qq] : ce;
+                                const int ts = lt ? bs[qq] : cs;
+                                if (lt) { be[qq] = ce; bs[qq] = cs; }
+                                ce = te;
+                                cs = ts;
                             }
                         }
                     }
