@@ -207,7 +207,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const int f0 = n * kBM + (int)rank * (kBM / 2);
                             const int lz = it.lb / a.B;
                             if (a.fused_gate) {
-                                um::tma_load_4d_pair(sa, &tmA0, bar, kx, f0, lz, 0);
+                                um::tma_load_3d_pair(sa, &tmA0, bar, kx, lz * a.d_ff + f0, 0);
                             } else {
                                 um::tma_load_3d_pair(sa, &tmA0, bar, kx, f0, lz);
                                 um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, f0, lz);
@@ -579,19 +579,19 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
     return r == CUDA_SUCCESS;
 }
 
-// W_c1 and W_c2 ([L][d_ff][W] each) seen as one [2][L][d_ff][W] tensor whose matrix
-// stride is the distance between them: box = 64 (inner) x 64 rows x 1 layer x both
+// W_c1 and W_c2 ([L][d_ff][W] each, i.e. [L*d_ff][W]) seen as one [2][L*d_ff][W] tensor
+// whose matrix stride is the distance between them: box = 64 (inner) x 64 rows x both
 // matrices, i.e. 64 rows of W_c1 followed by the same 64 rows of W_c2.
 static bool make_map_gates(CUtensorMap *m, const void *W1, long long gate_off, uint64_t inner,
                            uint64_t rows, uint64_t layers)
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[4] = {inner, rows, layers, 2};
-    cuuint64_t strides[3] = {inner * 2, inner * 2 * rows, (cuuint64_t)gate_off};
-    cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)(kBM / 2), 1, 2};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(W1), dims, strides,
+    cuuint64_t dims[3] = {inner, rows * layers, 2};
+    cuuint64_t strides[2] = {inner * 2, (cuuint64_t)gate_off};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)(kBM / 2), 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(W1), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
