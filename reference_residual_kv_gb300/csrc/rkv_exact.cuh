@@ -51,6 +51,19 @@ __device__ __forceinline__ float warp_tree_sum(float v)
     return v;
 }
 
+// Adds the squares of the eight bf16 values of one 16-byte word to acc, in element order.
+__device__ __forceinline__ float bf16x8_sqsum(const uint4 &v, float acc)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xffff0000u);
+        acc = fmaf(a, a, acc);
+        acc = fmaf(b, b, acc);
+    }
+    return acc;
+}
+
 template <typename TX, typename TR>
 __device__ __forceinline__ float sq8(const TX *x, const TR *r)
 {

@@ -92,7 +92,6 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
                                  int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
                                  int32_t *scan_count, int32_t *status, cudaStream_t s);
 // ||x||^2 of every token row (bf16 kv)
-cudaError_t launch_token_norms(const Geometry &g, const void *kv, float *xnorm, cudaStream_t s);
 
 int device_sm_count();
 

@@ -319,56 +319,6 @@ k_topk_fullscan(const T *__restrict__ kv, const T *__restrict__ refs,
     }
 }
 
-// ||x||^2 of every bf16 token row: one warp per row, all of a lane's 16-byte loads in
-// flight at once (the distance bound of the top-k finalisation needs it).
-template <int NV>
-__global__ void __launch_bounds__(256)
-k_token_norms(const __nv_bfloat16 *__restrict__ kv, long long rows, int W, float *__restrict__ out)
-{
-    const int lane = threadIdx.x & 31;
-    const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (r >= rows) return;
-    const __nv_bfloat16 *x = kv + (size_t)r * W;
-    float acc = 0.0f;
-    if constexpr (NV > 0) {
-        uint4 v[NV];
-#pragma unroll
-        for (int u = 0; u < NV; ++u) v[u] = __ldg((const uint4 *)(x + lane * 8 + u * 256));
-#pragma unroll
-        for (int u = 0; u < NV; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xffff0000u);
-                acc = fmaf(a, a, acc);
-                acc = fmaf(b, b, acc);
-            }
-        }
-    } else {
-        acc = 0.0f;
-        for (int c = lane * 8; c < W; c += 256) {
-            float a[8];
-            Vec8<__nv_bfloat16>::load(x + c, a);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc = fmaf(a[j], a[j], acc);
-        }
-    }
-    acc = warp_tree_sum(acc);
-    if (lane == 0) out[r] = acc;
-}
-
-cudaError_t launch_token_norms(const Geometry &g, const void *kv, float *xnorm, cudaStream_t s)
-{
-    const long long rows = (long long)g.LB * g.T;
-    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-    ProfScope prof("token_norms", s);
-    const __nv_bfloat16 *x = (const __nv_bfloat16 *)kv;
-    if (g.W == 2048) k_token_norms<8><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
-    else if (g.W == 1024) k_token_norms<4><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
-    else k_token_norms<0><<<blocks, 256, 0, s>>>(x, rows, g.W, xnorm);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *ref_exact,
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
                                  const float2 *cand, const float *xnorm, const float *rn_max,

@@ -11,6 +11,10 @@
 //   warp 1      TMEM allocation (both CTAs, 512 columns = two 256-column
 //               accumulators); MMA issue (leader only)
 //   warps 2..9  epilogue: TMEM lane quarter q = warp % 4, column half h
+//   warps 10..13 (M_DIST only) ||x||^2 of every token row, read from the token
+//               tiles in shared memory on each token tile's first N tile while the
+//               MMA works; a stage is free once the MMA and these warps are done
+//               with it (the top-k finalisation's distance bound needs the norms)
 // The epilogue is what differs between the four uses:
 //   M_P    P1 | P2 = R W_c1^T | R W_c2^T for each stored reference (fp32 out)
 //   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kList per row
@@ -28,6 +32,7 @@
 // projections and its stores are 128-byte lines.
 // Every mbarrier wait is bounded; on expiry the kernel reports
 // RKV_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and returns.
+#include "rkv_exact.cuh"
 #include "rkv_internal.cuh"
 #include "umma.cuh"
 
@@ -43,6 +48,8 @@ constexpr int kBBytes = kHalfN * kBK * 2;        // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // per CTA
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kNormWarps = 4;                    // M_DIST: token-norm warps per CTA
+template <int MODE> constexpr int threads_of() { return kThreads + (MODE == M_DIST ? 32 * kNormWarps : 0); }
 constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epilogue warp
 constexpr int kS1Round = 8;                      // S1: tokens whose gathers are in flight at once
 constexpr int kXTok = 16;                        // S1: tokens per exchange between warp pairs
@@ -76,6 +83,8 @@ struct UmmaArgs {
     float2 *hdr;
     float *z_out;
     int32_t *status;
+    const __nv_bfloat16 *xrows;   // M_DIST: the token rows (bf16, [LB*T][W]) ...
+    float *xnorm;                 // ... and their ||x||^2, written by the norm warps
 };
 
 // One work item of a pair: (lb, token tile t of 256 rows, N range [n0, n1)).
@@ -126,7 +135,7 @@ __device__ __forceinline__ float silu_fast(float u)
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmB, const UmmaArgs a)
 {
@@ -139,7 +148,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;                                // leader's: both epilogues
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    uint64_t *landed = drain + 1;                                // M_DIST, peer: stage landed
+    uint32_t *tmem_slot = (uint32_t *)(landed + S);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     int4 *info_buf = (int4 *)(tiles + S * kStageBytes + 256);
     float *xbuf = (float *)(tiles + S * kStageBytes + 256 + kInfoBytes);
@@ -150,13 +160,16 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             um::mbar_init(&full[s], 1);
-            um::mbar_init(&empty[s], 1);
+            // M_DIST: the MMA's commit and one arrival per norm warp
+            um::mbar_init(&empty[s], MODE == M_DIST ? 1 + kNormWarps : 1);
         }
         for (int b = 0; b < 2; ++b) {
             um::mbar_init(&tfull[b], 1);
             um::mbar_init(&tempty[b], 2 * kEpiWarps);
         }
         um::mbar_init(drain, 1);
+        if (MODE == M_DIST)
+            for (int s = 0; s < S; ++s) um::mbar_init(&landed[s], 1);
         *abort_flag = 0;
         um::fence_mbar_init();
     }
@@ -283,6 +296,54 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // all issued MMAs complete before TMEM can be released
             um::mma2_commit_mc(drain, 1);
             um::mbar_wait(drain, 0, kWaitCycles);
+        }
+    } else if (MODE == M_DIST && warp >= 2 + kEpiWarps) {
+        // ------------------------------------------------------------ token norms
+        // Every stage use, in the producer's order: wait until its copies have landed
+        // (the leader: its full barrier, which counts both CTAs' bytes; the peer: the
+        // leader's forward of it), read it if it is part of a token tile's first N
+        // tile, then add this warp's arrival to the stage's release.  Lane l of norm
+        // warp w owns token row 32w + l of this CTA's 128 A rows; a stage holds 64 of
+        // its values (one 128-byte row, 16-byte chunk c at position c ^ (row % 8), the
+        // 128-byte swizzle).  ||x||^2 is a sum over stages of per-stage sums of squares.
+        const int nrow = (warp - 2 - kEpiWarps) * 32 + lane;
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int i = pid; i < n_items && ok; i += npairs) {
+            Item it;
+            if (!item_get<MODE>(a, i, it)) continue;
+            for (int n = it.n0; n < it.n1 && ok; ++n) {
+                const bool need = it.chunk == 0 && n == 0;
+                float acc = 0.0f;
+                for (int kc = 0; kc < k_iters; ++kc) {
+                    const bool w = um::mbar_wait(leader ? &full[stage] : &landed[stage], ph, kWaitCycles);
+                    if (*abort_flag || !w) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader && warp == 2 + kEpiWarps && lane == 0)
+                        um::mbar_arrive_cluster_relaxed(um::mapa(um::smem_u32(&landed[stage]), 1));
+                    if (need) {
+                        const uint8_t *rowp = tiles + stage * kStageBytes + nrow * 128;
+                        float part[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            part[c] = bf16x8_sqsum(*(const uint4 *)(rowp + ((c ^ (nrow & 7)) << 4)), 0.0f);
+                        acc += ((part[0] + part[1]) + (part[2] + part[3])) +
+                               ((part[4] + part[5]) + (part[6] + part[7]));
+                    }
+                    __syncwarp();
+                    if (lane == 0) um::mbar_arrive(&empty[stage]);
+                    if (++stage == S) { stage = 0; ph ^= 1u; }
+                }
+                const int r = it.t * 2 * kBM + (int)rank * kBM + nrow;
+                if (need && ok && r < a.rows) a.xnorm[(size_t)it.lb * a.T + r] = acc;
+            }
+        }
+        if (!ok) {
+            set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -618,7 +679,7 @@ static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUten
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_of<MODE>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = at;
@@ -653,6 +714,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     const bool fp8 = g.ref_dtype == RKV_FP8_E4M3;
     void *ref_mma = fp8 ? (void *)(ws + wl.ref_mma) : pool->ref_vec;
     const size_t zrow = (size_t)g.LB * g.n_ref * g.d_ff;     // the all-zero projection row
+    float *xnorm = (float *)(ws + wl.xnorm);
     if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, P1 + zrow, P2 + zrow, s)) != cudaSuccess)
         return e;
 
@@ -698,11 +760,10 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         UmmaArgs d = a;
         d.rows = g.T; d.tiles_t = g.n_mtiles; d.tiles_n = g.max_chunks;
         d.k_chunks = kw; d.a_sources = 1;
+        d.xrows = (const __nv_bfloat16 *)kv; d.xnorm = xnorm;
         if ((e = run<M_DIST>(mX, mX, mR, d, s)) != cudaSuccess) return e;
     }
     int32_t *scan_list = (int32_t *)(ws + wl.scan_list);
-    float *xnorm = (float *)(ws + wl.xnorm);
-    if (g.n_ref > 0 && (e = launch_token_norms(g, kv, xnorm, s)) != cudaSuccess) return e;
     if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, xnorm, rn_max, cache->ref_idx,
                                   copy_flag, scan_list, scan_list + (size_t)g.LB * g.T, status,
                                   s)) != cudaSuccess)
