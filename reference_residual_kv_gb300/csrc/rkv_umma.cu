@@ -52,16 +52,18 @@ constexpr int kNormWarps = 4;                    // M_DIST: token-norm warps per
 template <int MODE> constexpr int threads_of() { return kThreads + (MODE == M_DIST ? 32 * kNormWarps : 0); }
 constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epilogue warp
 constexpr int kS1Round = 8;                      // S1: tokens whose gathers are in flight at once
-constexpr int kXTok = 16;                        // S1: tokens per exchange between warp pairs
+constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
 constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(2 * kBM, kBN);
 constexpr uint16_t kPairMask = 3;
 
 template <int MODE> struct Cfg {
     static constexpr bool kT = MODE == M_P || MODE == M_S1;   // transposed
-    static constexpr int kStages = MODE == M_S1 ? 5 : 6;
+    static constexpr int kStages = MODE == M_S1 || MODE == M_DIST ? 6 : 7;
     static constexpr int kExtra = MODE == M_S1 ? kInfoBytes + kXBytes : 0;
     static constexpr int kSmem = kStages * kStageBytes + 1024 + 256 + kExtra;
+    static_assert(kSmem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
+    static_assert((3 * kStages + 5) * 8 + 8 <= 256, "barriers overflow their 256-byte block");
 };
 
 struct UmmaArgs {

@@ -35,12 +35,15 @@ def _attend(cfg, q_bits, k_bits, v_bits, sel):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,n_sel", [
-    ("llama3.1-8b-kv", 1200),      # 32 query heads on 8 KV heads; 3 splits, ragged
-    ("qwen2.5-7b-kv", 700),        # 28 query heads on 4 KV heads (groups of 7)
+@pytest.mark.parametrize("name,n_sel,shape", [
+    ("llama3.1-8b-kv", 1200, {}),                      # 32 query heads on 8 KV heads; ragged batches
+    ("qwen2.5-7b-kv", 700, {}),                        # 28 query heads on 4 KV heads (groups of 7)
+    ("llama3.1-8b-kv", 333, dict(N=16, D=64)),         # D = 64, groups of 2
+    ("llama3.1-8b-kv", 517, dict(N=4, D=64)),          # D = 64, groups of 8
+    ("llama3.1-8b-kv", 901, dict(N=4, D=256, H=16)),   # D = 256, groups of 4
 ])
-def test_attention_matches_oracle(name, n_sel):
-    cfg = C[name].replace(L=2, T=4096)
+def test_attention_matches_oracle(name, n_sel, shape):
+    cfg = C[name].replace(L=2, T=4096, **shape)
     dk = cfg.N * cfg.D
     kv = [wl.layer_kv(cfg, l)[0] for l in range(cfg.L)]           # rows stand in for K^ | V^
     rng = np.random.default_rng(n_sel)
