@@ -425,6 +425,10 @@ def run_ours(args, cfg):
     from reference_residual_kv_gb300 import rkv
     rkv_build.build()
     rkv.lib()
+    if args.read_path_only:
+        # the long-context read path alone (small cases for a profiler)
+        print(json.dumps({"read_path": read_path(dev, steps=args.read_steps)}), flush=True)
+        return
 
     kv, w = _gen_inputs(cfg)
     kv_h = torch.from_numpy(np.stack(kv).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -562,7 +566,7 @@ def run_ours(args, cfg):
         line["decode_write"] = decode_write(cfg, bufs, kv_d, W1, W2, W3, dev)
         del kv_d, G, W1, W2, W3, bufs, out_z, out_m
         torch.cuda.empty_cache()
-        line["read_path"] = read_path(dev)
+        line["read_path"] = read_path(dev, steps=args.read_steps)
     if not args.no_cpu_baseline and ws >= 1:
         line["cpu_baseline"] = cpu_baseline(cfg)
     print(json.dumps(line), flush=True)
@@ -581,6 +585,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-read-path", action="store_true",
                     help="skip the long-context sparse-read measurement")
+    ap.add_argument("--read-path-only", action="store_true",
+                    help="run only the long-context sparse-read measurement")
+    ap.add_argument("--read-steps", type=int, default=256,
+                    help="decode steps of the sparse-read measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

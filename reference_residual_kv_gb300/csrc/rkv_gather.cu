@@ -13,40 +13,57 @@
 
 namespace rkv {
 
-// Adds 8 consecutive reference values into 4 float2 accumulators with paired fp32
-// adds (one IEEE add per element, same order as scalar code).
+// Adds 8 consecutive reference values into 8 fp32 accumulators: one IEEE add per
+// element of its exact widening, in the same order as scalar code (bf16 and fp16
+// operands go straight into the fp32 add).
+__device__ __forceinline__ void add_bf16x2(uint32_t w, float &a0, float &a1)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
+}
+__device__ __forceinline__ void add_f16x2(uint32_t w, float &a0, float &a1)
+{
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
+}
+
 template <typename T> struct RefLoad;
 template <> struct RefLoad<float> {
-    static __device__ __forceinline__ void add(const float *p, float2 (&a)[4])
+    static __device__ __forceinline__ void add(const float *p, float (&a)[8])
     {
         const float4 u = *(const float4 *)p, v = *(const float4 *)(p + 4);
-        a[0] = __fadd2_rn(a[0], make_float2(u.x, u.y));
-        a[1] = __fadd2_rn(a[1], make_float2(u.z, u.w));
-        a[2] = __fadd2_rn(a[2], make_float2(v.x, v.y));
-        a[3] = __fadd2_rn(a[3], make_float2(v.z, v.w));
+        const float x[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const float2 r = __fadd2_rn(make_float2(a[j], a[j + 1]), make_float2(x[j], x[j + 1]));
+            a[j] = r.x;
+            a[j + 1] = r.y;
+        }
     }
 };
 template <> struct RefLoad<__nv_bfloat16> {
-    static __device__ __forceinline__ void add(const __nv_bfloat16 *p, float2 (&a)[4])
+    static __device__ __forceinline__ void add(const __nv_bfloat16 *p, float (&a)[8])
     {
         const uint4 raw = *(const uint4 *)p;
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)     // bf16 -> fp32 is a 16-bit shift
-            a[j] = __fadd2_rn(a[j], make_float2(__uint_as_float(w[j] << 16),
-                                                __uint_as_float(w[j] & 0xffff0000u)));
+        for (int j = 0; j < 4; ++j) add_bf16x2(w[j], a[2 * j], a[2 * j + 1]);
     }
 };
 template <> struct RefLoad<uint8_t> {     // FP8 E4M3: exact in fp16, two per conversion
-    static __device__ __forceinline__ void add(const uint8_t *p, float2 (&a)[4])
+    static __device__ __forceinline__ void add(const uint8_t *p, float (&a)[8])
     {
         const uint2 raw = *(const uint2 *)p;
         const uint32_t w[2] = {raw.x, raw.y};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[j >> 1] >> (16 * (j & 1))) & 0xffffu);
-            const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
-            a[j] = __fadd2_rn(a[j], __half22float2(h));
+            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+            add_f16x2((uint32_t)h2.x | ((uint32_t)h2.y << 16), a[2 * j], a[2 * j + 1]);
         }
     }
 };
@@ -88,6 +105,18 @@ k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int 
     int slots[4] = {-1, -1, -1, -1};
     int k = 0;
     const size_t rec = (size_t)lb * T + (ok ? t : 0);
+    // the record's codes and extremes are loaded with its reference slots, before any
+    // of them is used (the first of at most two code words and extremes per lane)
+    const int pitch = d_c * bits / 8;
+    const uint8_t *crow = codes + rec * pitch;
+    const float2 *hrow = hdr + rec * (d_c / 32);
+    uint32_t word0 = 0;
+    float2 h0 = make_float2(0.0f, 0.0f);
+    if (ok && lane * 8 < d_c) {
+        h0 = __ldg(hrow + ((lane * 8) >> 5));
+        word0 = bits == 4 ? __ldg((const uint32_t *)(crow + ((lane * 8) >> 1)))
+                          : (uint32_t)__ldg((const uint16_t *)(crow + ((lane * 8) >> 2)));
+    }
     if (ok) {
         int4 ix = __ldg(ref_idx + rec);
         slots[0] = ix.x; slots[1] = ix.y; slots[2] = ix.z; slots[3] = ix.w;
@@ -104,14 +133,14 @@ k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int 
     }
 
     // z~: each lane decodes 8 coordinates per step
-    const int pitch = d_c * bits / 8;
-    const uint8_t *crow = codes + rec * pitch;
-    const float2 *hrow = hdr + rec * (d_c / 32);
     for (int c = lane * 8; c < d_c; c += 256) {
-        float2 h = __ldg(hrow + (c >> 5));
-        uint32_t word;
-        if (bits == 4) word = __ldg((const uint32_t *)(crow + (c >> 1)));
-        else word = (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
+        float2 h = h0;
+        uint32_t word = word0;
+        if (c >= 256) {
+            h = __ldg(hrow + (c >> 5));
+            word = bits == 4 ? __ldg((const uint32_t *)(crow + (c >> 1)))
+                             : (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
+        }
         float v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -127,15 +156,13 @@ k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int 
     const float2 ik2 = make_float2(inv_k, inv_k);
 #pragma unroll 4
     for (int c = lane * 8; c < W; c += 256) {
-        float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                        make_float2(0.f, 0.f)};
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a2);
-        float a[8];
+            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float2 m = __fmul2_rn(a2[j], ik2);
+            const float2 m = __fmul2_rn(make_float2(a[2 * j], a[2 * j + 1]), ik2);
             a[2 * j] = m.x;
             a[2 * j + 1] = m.y;
         }

@@ -10,11 +10,12 @@
 //   warp 0      TMA producer (both CTAs): this CTA's 128 rows of W_d (out-major) per
 //               64-wide K chunk; both CTAs' copies complete on the leader's barrier
 //   warp 1      TMEM allocation (both CTAs); MMA issue (leader)
-//   warps 2..9  per item (256 selected tokens of one layer-sequence): first write the
-//               CTA's 128 rows of z~ (dequantised codes, bf16) into shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, resident for all N tiles;
-//               then, per N tile, read the accumulator, add the reference mean, rotate
-//               key pairs and store bf16.
+//   warps 2..9  per item (256 selected tokens of one layer-sequence and a group of
+//               consecutive N tiles): first write the CTA's 128 rows of z~ (dequantised
+//               codes, bf16) into shared memory in the 128-byte-swizzled K-major layout
+//               the MMA reads, resident for the group's N tiles; then, per N tile, read
+//               the accumulator, add the reference mean, rotate key pairs and store bf16.
+// Items split the N tiles into groups when that evens out the rounds of the pairs.
 // Every mbarrier wait is bounded; on expiry the kernel reports RKV_ERR_DEVICE_TIMEOUT.
 #include "rkv_internal.cuh"
 #include "umma.cuh"
@@ -38,6 +39,7 @@ constexpr int kMaxPairs = 128;                 // D <= 256
 struct RestoreArgs {
     int LB, B, T, n_sel, W, dk, D, d_c, bits, n_ref, ref_fp8;
     int tiles_t, n_tiles, k_chunks;
+    int n_groups, group_tiles;                 // an item: one token tile x group_tiles N tiles
     const int32_t *sel;
     const uint8_t *codes;
     const float2 *hdr;
@@ -148,7 +150,8 @@ template <bool FP8> struct RefChunk {
         }
     }
 
-    // fp32 sum in ascending slot order; FP8 decodes exactly through fp16
+    // fp32 sum in ascending slot order: each value enters as one add of its exact
+    // widening (FP8 E4M3 through fp16, bf16 directly) to the fp32 accumulator
     __device__ __forceinline__ void sum(const int (&slot)[4], float (&m)[32]) const
     {
 #pragma unroll
@@ -163,16 +166,20 @@ template <bool FP8> struct RefChunk {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-                        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-                        m[v * 16 + 2 * e] += f.x;
-                        m[v * 16 + 2 * e + 1] += f.y;
+                        const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                        const uint32_t hw = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
+                        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                            "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+                            : "+f"(m[v * 16 + 2 * e]), "+f"(m[v * 16 + 2 * e + 1])
+                            : "r"(hw));
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        m[v * 8 + 2 * e] += __uint_as_float(wv[e] << 16);
-                        m[v * 8 + 2 * e + 1] += __uint_as_float(wv[e] & 0xffff0000u);
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                            "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+                            : "+f"(m[v * 8 + 2 * e]), "+f"(m[v * 8 + 2 * e + 1])
+                            : "r"(wv[e]));
                 }
             }
         }
@@ -220,7 +227,7 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
     um::cluster_sync();
     um::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = a.LB * a.tiles_t;
+    const int n_items = a.LB * a.tiles_t * a.n_groups;
     const int pid = blockIdx.x / 2, npairs = gridDim.x / 2;
 
     if (warp == 0) {
@@ -234,8 +241,9 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
             for (int s = 0; s < kStages; ++s) { used[s] = false; last_ph[s] = 0; }
             bool ok = true;
             for (int i = pid; i < n_items && ok; i += npairs) {
-                const int lz = (i / a.tiles_t) / a.B;
-                for (int n = 0; n < a.n_tiles && ok; ++n) {
+                const int lz = (i / a.n_groups / a.tiles_t) / a.B;
+                const int nb = (i % a.n_groups) * a.group_tiles;
+                for (int n = nb; n < nb + a.group_tiles && ok; ++n) {
                     for (int kc = 0; kc < a.k_chunks; ++kc) {
                         const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles);
                         if (*abort_flag || !w) { ok = false; break; }
@@ -269,7 +277,7 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                 const bool wz = um::mbar_wait(zready, ic & 1u, kWaitCycles);
                 if (*abort_flag || !wz) { ok = false; break; }
                 um::tc_fence_after();
-                for (int n = 0; n < a.n_tiles && ok; ++n) {
+                for (int n = 0; n < a.group_tiles && ok; ++n) {
                     const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
                     const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles);
                     if (*abort_flag || !w) { ok = false; break; }
@@ -309,7 +317,8 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
         uint32_t cnt = 0;
         bool ok = true;
         for (int i = pid; i < n_items; i += npairs) {
-            const int lb = i / a.tiles_t, t = i % a.tiles_t;
+            const int lb = i / a.n_groups / a.tiles_t, t = (i / a.n_groups) % a.tiles_t;
+            const int nb = (i % a.n_groups) * a.group_tiles, ne = nb + a.group_tiles;
             const int e0 = t * 2 * kBM + (int)rank * kBM;   // this CTA's first selected entry
             // (1) this warp's 16 rows of the CTA's z~ tile: every load first (the rows'
             // positions, then their codes and extremes), then dequantise and write
@@ -359,9 +368,8 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
             // (3) the N tiles' accumulators; the next chunk's reference values are
             // loaded while this chunk is rotated and stored
             RefChunk<FP8> rch;
-            const int n_chunks = a.n_tiles * 4;
-            if (okt) rch.load(a, slot, lb, h * (kBN / 2));
-            for (int n = 0; n < a.n_tiles; ++n) {
+            if (okt) rch.load(a, slot, lb, nb * kBN + h * (kBN / 2));
+            for (int n = nb; n < ne; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
                 bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -377,11 +385,17 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                         // KV^ = f_d(z~) + (sum of the references) * 1/k
                         float m[32];
                         rch.sum(slot, m);
+                        const float2 ik2 = make_float2(inv_k, inv_k);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = fmaf(m[j], inv_k, o[j]);
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 r = __ffma2_rn(make_float2(m[2 * j], m[2 * j + 1]), ik2,
+                                                        make_float2(o[2 * j], o[2 * j + 1]));
+                            o[2 * j] = r.x;
+                            o[2 * j + 1] = r.y;
+                        }
                     }
                     const int g1 = n * 4 + cc + 1;
-                    if (okt && g1 < n_chunks)
+                    if (okt && g1 < ne * 4)
                         rch.load(a, slot, lb, (g1 >> 2) * kBN + h * (kBN / 2) + (g1 & 3) * 32);
                     if (e >= a.n_sel) continue;
                     const bool is_k = c0 < a.dk;
@@ -394,8 +408,11 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                                 float cs, sn;
                                 rope_cs(pos, a.theta[p0 + j], cs, sn);
                                 const float x0 = o[2 * j], x1 = o[2 * j + 1];
-                                o[2 * j] = x0 * cs - x1 * sn;
-                                o[2 * j + 1] = x0 * sn + x1 * cs;
+                                // (x0 cs - x1 sn, x1 cs + x0 sn)
+                                const float2 r = __ffma2_rn(make_float2(-x1, x0), make_float2(sn, sn),
+                                                            __fmul2_rn(make_float2(x0, x1), make_float2(cs, cs)));
+                                o[2 * j] = r.x;
+                                o[2 * j + 1] = r.y;
                             }
                         }
                     } else {
@@ -448,6 +465,8 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     a.ref_fp8 = g.ref_dtype == RKV_FP8_E4M3;
     a.tiles_t = (n_sel + kTileM - 1) / kTileM;
     a.n_tiles = g.W / kBN;
+    a.n_groups = 1;
+    a.group_tiles = a.n_tiles;
     a.k_chunks = g.d_c / kBK;
     a.sel = sel; a.codes = cache->codes; a.hdr = (const float2 *)cache->hdr;
     a.ref_idx = (const int4 *)cache->ref_idx; a.ref_vec = pool->ref_vec;
@@ -467,8 +486,7 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
         if (e != cudaSuccess) return e;
         attr[a.ref_fp8] = true;
     }
-    const long long items = (long long)g.LB * a.tiles_t;
-    if (items <= 0) return cudaSuccess;
+    if ((long long)g.LB * a.tiles_t <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -486,6 +504,20 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
         cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)kern, &cfg);
         if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
     }
+    // N-tile groups: the split whose rounds of items over the pairs, each costing its
+    // tiles plus about half a tile for writing the z~ tile, finish first
+    {
+        const long long base = (long long)g.LB * a.tiles_t;
+        double best = 0.0;
+        for (int ng = 1; ng <= a.n_tiles; ng *= 2) {
+            if (a.n_tiles % ng) continue;
+            const long long rounds = (base * ng + max_pairs - 1) / max_pairs;
+            const double cost = (double)rounds * ((double)(a.n_tiles / ng) + 0.5);
+            if (ng == 1 || cost < best) { best = cost; a.n_groups = ng; }
+        }
+        a.group_tiles = a.n_tiles / a.n_groups;
+    }
+    const long long items = (long long)g.LB * a.tiles_t * a.n_groups;
     const long long np = items < max_pairs ? items : max_pairs;
     cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
     ProfScope prof("restore_kv", s);
