@@ -39,8 +39,8 @@ UNIT = "tokens/s"
 # this workload, from one `ncu --set full` capture of the 4-layer case scaled to 32
 # layers by the units processed (its traffic grows in proportion).  Set an entry to None
 # when its kernel changes.
-NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (200.954368e6 + 108.118528e6),
-                  "umma_distance_topk": 8 * (165.357312e6 + 4.224256e6)}
+NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (201.037056e6 + 108.294400e6),
+                  "umma_distance_topk": 8 * (174.959360e6 + 6.633728e6)}
 
 
 def _peaks():
