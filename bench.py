@@ -255,7 +255,9 @@ def run_reference(args, cfg):
 def read_path(dev, steps=256, reps=3):
     """The sparse read on the long-context workload (131072 tokens, FP8 references):
     `steps` decode steps, each reading 30% random tokens plus the last 512, captured in
-    one CUDA graph; plus that workload's compress rate.  Inputs are device-resident."""
+    one CUDA graph; plus that workload's compress rate, the restore and attention of the
+    same selections, and the decode loop (append + gather + restore + attention per
+    step).  Inputs are device-resident."""
     import torch
     from reference_residual_kv_gb300 import rkv
     cfg = wl.CONFIGS["long-131k-fp8ref"]
@@ -361,6 +363,40 @@ def read_path(dev, steps=256, reps=3):
                "frac_of_sustained": r_flops / (r_ms / 1e3) / 1e12 / tf_sust,
                "bytes_per_step": r_bytes, "achieved_gbs": r_bytes / (r_ms / 1e3) / 1e9,
                "device_status": bufs.device_status()}
+    # the decode loop: each of `steps` steps appends the next token (the last `steps`
+    # positions of the sequence, encoded against the pool before them), gathers the
+    # step's selection, restores its K^ and V^ and attends over them; one CUDA graph
+    t0 = cfg.T - steps
+    kv_rows = kv.view(cfg.T, -1)
+    xs = [kv_rows[t0 + s_].view(1, -1).contiguous() for s_ in range(steps)]
+
+    def decode_step(s_):
+        sl = sels[s_].view(1, -1)
+        bufs.append(xs[s_], t0 + s_, W1, W2, W3, stream=side)
+        bufs.gather(sl, oz, om, stream=side)
+        bufs.restore(Wd, sl, ok_, ov_, cfg.rope_base, stream=side)
+        bufs.attend(cfg.H, qs[s_ % r_steps], ok_, ov_, sl, ao, stream=side)
+
+    with torch.cuda.stream(side):
+        decode_step(0)
+    side.synchronize()
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=side):
+        for s_ in range(steps):
+            decode_step(s_)
+    gd.replay()
+    torch.cuda.synchronize(dev)
+    d_reps = 2
+    a.record(stream)
+    for _ in range(d_reps):
+        gd.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    d_ms = a.elapsed_time(b) / (d_reps * steps)
+    decode_loop = {"workload": "long-131k-fp8ref: %d decode steps, each: append token t (the last %d "
+                               "positions), gather ~%d selected tokens, restore their K^/V^ (RoPE), "
+                               "attention of %d query heads; one CUDA graph" % (steps, steps, int(n_tok), cfg.H),
+                   "ms_per_step": d_ms, "steps_per_s": 1e3 / d_ms, "device_status": bufs.device_status()}
     per_tok = gather_bytes_per_token(cfg)
     ref_bytes = bufs.n_ref * cfg.W * 1
     bytes_step = n_tok * per_tok + ref_bytes
@@ -374,7 +410,8 @@ def read_path(dev, steps=256, reps=3):
             "unit": "GB/s", "frac": gbs / hbm, "peak_source": "%s HBM copy bandwidth" % src,
             "device_status": st,
             "compress_tokens_per_s": cfg.T / (c_ms / 1e3), "compress_ms": c_ms,
-            "compress_kernels_ms": c_prof, "restore": restore, "attention": attention}
+            "compress_kernels_ms": c_prof, "restore": restore, "attention": attention,
+            "decode_loop": decode_loop}
 
 
 def decode_write(cfg, bufs, kv_d, W1, W2, W3, dev, calls=20, reps=3):

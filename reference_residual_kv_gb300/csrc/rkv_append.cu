@@ -64,8 +64,17 @@ k_app_dist(const TX *__restrict__ kv_new, int t, const int32_t *__restrict__ ref
     int bs[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = kNoSlot; }
-    for (int m = m0 + warp; m < m1; m += 8)
-        list_insert<kMaxK>(be, bs, warp_sqdist(x, rb + (size_t)m * W, W, lane), m);
+    // two of the warp's references at a time (their loads in flight together)
+    for (int m = m0 + warp; m < m1; m += 16) {
+        if (m + 8 < m1) {
+            float d0, d1;
+            warp_sqdist2(x, rb + (size_t)m * W, rb + (size_t)(m + 8) * W, W, lane, d0, d1);
+            list_insert<kMaxK>(be, bs, d0, m);
+            list_insert<kMaxK>(be, bs, d1, m + 8);
+        } else {
+            list_insert<kMaxK>(be, bs, warp_sqdist(x, rb + (size_t)m * W, W, lane), m);
+        }
+    }
     if (lane == 0) {
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) { sd[warp][j] = be[j]; ss[warp][j] = bs[j]; }
@@ -106,11 +115,30 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
              const float2 *__restrict__ part, int4 *__restrict__ ref_idx, float *__restrict__ mean,
              int *__restrict__ state)
 {
+    constexpr int kStage = 1024;  // slice entries staged in shared memory per round
+    __shared__ float2 pe[kStage];
     __shared__ int ch[kMaxK];
     __shared__ int info[2];       // k_t, state
     const int lb = blockIdx.x;
+    const int own = ref_slot[t];
+    float fe[kMaxK];
+    int fs[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) { fe[j] = INFINITY; fs[j] = kNoSlot; }
+    if (own < 0) {
+        // the slices' candidates: all threads stage them, thread 0 merges them in order
+        const int total = ((pool_size[t] + kSlice - 1) / kSlice) * kMaxK;
+        const float2 *src = part + (size_t)lb * slices * kMaxK;
+        for (int base = 0; base < total; base += kStage) {
+            const int cnt = min(kStage, total - base);
+            __syncthreads();
+            for (int i = threadIdx.x; i < cnt; i += blockDim.x) pe[i] = src[base + i];
+            __syncthreads();
+            if (threadIdx.x == 0)
+                for (int i = 0; i < cnt; ++i) list_insert<kMaxK>(fe, fs, pe[i].x, __float_as_int(pe[i].y));
+        }
+    }
     if (threadIdx.x == 0) {
-        const int own = ref_slot[t];
         int c[kMaxK] = {kNoSlot, kNoSlot, kNoSlot, kNoSlot};
         int kt = 0, st = 0;
         if (own >= 0) {
@@ -118,17 +146,6 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
             st = 1;
         } else {
             const int pool = pool_size[t];
-            float fe[kMaxK];
-            int fs[kMaxK];
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) { fe[j] = INFINITY; fs[j] = kNoSlot; }
-            const int ns = (pool + kSlice - 1) / kSlice;
-            for (int s = 0; s < ns; ++s)
-#pragma unroll
-                for (int j = 0; j < kMaxK; ++j) {
-                    const float2 e = part[((size_t)lb * slices + s) * kMaxK + j];
-                    list_insert<kMaxK>(fe, fs, e.x, __float_as_int(e.y));
-                }
             kt = min(k, pool);
             bool same = kt > 0;
 #pragma unroll
@@ -156,9 +173,15 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
     if (info[1] != 0) return;
     const float inv = kt > 0 ? 1.0f / (float)kt : 0.0f;
     const TR *rb = ref_vec + (size_t)lb * n_ref * W;
+#pragma unroll 4
     for (int c = threadIdx.x; c < W; c += blockDim.x) {
+        float v[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) v[j] = j < kt ? ref_value(rb + (size_t)ch[j] * W + c) : 0.0f;
         float acc = 0.0f;
-        for (int j = 0; j < kt; ++j) acc += ref_value(rb + (size_t)ch[j] * W + c);
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+            if (j < kt) acc += v[j];
         mean[(size_t)lb * W + c] = acc * inv;
     }
 }
@@ -184,7 +207,9 @@ k_app_h(const TX *__restrict__ kv_new, const TX *__restrict__ W1t, const TX *__r
     const float *m = mean + (size_t)lb * W;
     const size_t wrow = ((size_t)(lb / B) * d_ff + f) * W;
     float a1 = 0.0f, a2 = 0.0f, b1 = 0.0f, b2 = 0.0f;
-    // 8 consecutive coordinates per lane and step (16-byte loads of bf16 rows)
+    // 8 consecutive coordinates per lane and step (16-byte loads of bf16 rows); four
+    // steps' loads in flight at once
+#pragma unroll 4
     for (int c = lane * 8; c < W; c += 256) {
         float w1[8], w2[8], xv[8], mv[8];
         Vec8<TX>::load(W1t + wrow + c, w1);
@@ -218,6 +243,7 @@ k_app_z(const TX *__restrict__ W3t, int d_ff, int d_c, int B, const float *__res
     const float *h = dh + (size_t)lb * d_ff;
     const TX *w = W3t + ((size_t)(lb / B) * d_c + j) * d_ff;
     float acc = 0.0f;
+#pragma unroll 4
     for (int f = lane * 8; f < d_ff; f += 256) {
         float hv[8], wv[8];
         Vec8<float>::load(h + f, hv);

@@ -96,6 +96,32 @@ __device__ __forceinline__ float warp_sqdist(const TX *x, const TR *r, int W, in
     return warp_tree_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
 
+// warp_sqdist of two rows against the same x, their loads interleaved; each result is
+// formed exactly as warp_sqdist forms it.
+template <typename TX, typename TR = TX>
+__device__ __forceinline__ void warp_sqdist2(const TX *x, const TR *r0, const TR *r1, int W, int lane,
+                                             float &d0, float &d1)
+{
+    float a0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int c = lane * 8;
+    for (; c + 3 * 256 < W; c += 4 * 256) {
+        float p0[4], p1[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            p0[u] = sq8(x + c + u * 256, r0 + c + u * 256);
+            p1[u] = sq8(x + c + u * 256, r1 + c + u * 256);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { a0[u] += p0[u]; a1[u] += p1[u]; }
+    }
+    for (; c < W; c += 256) {
+        a0[0] += sq8(x + c, r0 + c);
+        a1[0] += sq8(x + c, r1 + c);
+    }
+    d0 = warp_tree_sum((a0[0] + a0[1]) + (a0[2] + a0[3]));
+    d1 = warp_tree_sum((a1[0] + a1[1]) + (a1[2] + a1[3]));
+}
+
 __device__ __forceinline__ bool key_less(float ea, int sa, float eb, int sb)
 {
     return ea < eb || (ea == eb && (unsigned)sa < (unsigned)sb);
