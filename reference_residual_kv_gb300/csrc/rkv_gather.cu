@@ -4,9 +4,10 @@
 // code z~ = q*delta + z_min [RKV §2.4] and the reference mean in KV space [RKV §2.2].
 // Groups never span tokens [RKV §2.4], so no unselected neighbour is touched.
 //
-// One warp per selected token.  Records are read with 8/16-byte loads, references
-// with 16-byte loads (L2-resident: one sequence's pool is a few MB), outputs are
-// written with 16-byte stores.
+// Warps take one selected token at a time, persistent for bf16 and fp32 references
+// with the next token's record loaded ahead.  Records are read with 8/16-byte loads, references with 8/16-byte loads
+// (L2-resident: one sequence's pool is a few MB), outputs are written with 16-byte
+// stores.
 #include "rkv_internal.cuh"
 
 #include <cuda_fp16.h>
@@ -68,6 +69,13 @@ template <> struct RefLoad<uint8_t> {     // FP8 E4M3: exact in fp16, two per co
     }
 };
 
+// Launch shape by reference dtype (measured): bf16 and fp32 references run persistent
+// warps, 3 blocks per SM, each warp walking several tokens with the next token's record
+// loaded ahead; FP8 references (half the bytes per reference, more conversions) run one
+// warp per token at 5 blocks per SM with four mean steps' loads in flight.
+template <typename RefT> constexpr bool kPersistent = sizeof(RefT) != 1;
+template <typename RefT> constexpr int kGatherBlocks = kPersistent<RefT> ? 3 : 5;
+
 template <typename OutT>
 __device__ __forceinline__ void store8(OutT *dst, const float (&v)[8]);
 template <> __device__ __forceinline__ void store8<float>(float *dst, const float (&v)[8])
@@ -84,89 +92,140 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *dst, const 
     *(uint4 *)dst = *(const uint4 *)o;
 }
 
+// A selected token's record as a warp holds it: reference slots, and this lane's first
+// two code words and group extremes (d_c <= 512 needs no more).
+struct GRec {
+    int4 ix;
+    uint32_t w[2];
+    float2 h[2];
+};
+
+__device__ __forceinline__ GRec load_rec(int lane, int t, bool ok, size_t rec, int d_c, int bits,
+                                         const uint8_t *__restrict__ codes, const float2 *__restrict__ hdr,
+                                         const int4 *__restrict__ ref_idx)
+{
+    GRec r;
+    r.ix = make_int4(-1, -1, -1, -1);
+    r.w[0] = r.w[1] = 0u;
+    r.h[0] = r.h[1] = make_float2(0.0f, 0.0f);
+    if (!ok) return r;
+    r.ix = __ldg(ref_idx + rec);
+    const uint8_t *crow = codes + rec * (size_t)(d_c * bits / 8);
+    const float2 *hrow = hdr + rec * (size_t)(d_c / 32);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = lane * 8 + u * 256;
+        if (c < d_c) {
+            r.h[u] = __ldg(hrow + (c >> 5));
+            r.w[u] = bits == 4 ? __ldg((const uint32_t *)(crow + (c >> 1)))
+                               : (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
+        }
+    }
+    return r;
+}
+
+// Persistent: each warp takes the selected tokens gw, gw + nw, ... in turn, and loads the
+// next token's record and the position of the one after it before it decodes the
+// current one, so that the chain position -> record -> reference rows overlaps the work.
 template <typename RefT, typename OutT>
-__global__ void __launch_bounds__(256, 5)
+__global__ void __launch_bounds__(256, kGatherBlocks<RefT>)
 k_gather(const int32_t *__restrict__ sel, int n_sel, int T, int W, int d_c, int bits,
          int n_ref, const RefT *__restrict__ ref_vec, const uint8_t *__restrict__ codes,
          const float2 *__restrict__ hdr, const int4 *__restrict__ ref_idx, OutT *__restrict__ out_z,
          OutT *__restrict__ out_mean, long long total, int32_t *status)
 {
     const int lane = threadIdx.x & 31;
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (gw >= total) return;
-    const int lb = (int)(gw / n_sel);
-    const int t = __ldg(sel + gw);
-    OutT *oz = out_z + (size_t)gw * d_c;
-    OutT *om = out_mean + (size_t)gw * W;
+    const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+    long long tok = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (tok >= total) return;
     const float zero8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 
-    bool ok = t >= 0 && t < T;
-    if (t >= T) set_status(status, RKV_ERR_INDEX);
-    int slots[4] = {-1, -1, -1, -1};
-    int k = 0;
-    const size_t rec = (size_t)lb * T + (ok ? t : 0);
-    // the record's codes and extremes are loaded with its reference slots, before any
-    // of them is used (the first of at most two code words and extremes per lane)
-    const int pitch = d_c * bits / 8;
-    const uint8_t *crow = codes + rec * pitch;
-    const float2 *hrow = hdr + rec * (d_c / 32);
-    uint32_t word0 = 0;
-    float2 h0 = make_float2(0.0f, 0.0f);
-    if (ok && lane * 8 < d_c) {
-        h0 = __ldg(hrow + ((lane * 8) >> 5));
-        word0 = bits == 4 ? __ldg((const uint32_t *)(crow + ((lane * 8) >> 1)))
-                          : (uint32_t)__ldg((const uint16_t *)(crow + ((lane * 8) >> 2)));
-    }
-    if (ok) {
-        int4 ix = __ldg(ref_idx + rec);
-        slots[0] = ix.x; slots[1] = ix.y; slots[2] = ix.z; slots[3] = ix.w;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (slots[j] >= n_ref) { ok = false; set_status(status, RKV_ERR_INDEX); }
-            if (slots[j] >= 0) ++k;
+    int t = __ldg(sel + tok);
+    GRec rc = load_rec(lane, t, t >= 0 && t < T, (size_t)(tok / n_sel) * T + t, d_c, bits, codes, hdr, ref_idx);
+    long long tn = tok + nw;
+    int t_n = -1;
+    if constexpr (kPersistent<RefT>) t_n = tn < total ? __ldg(sel + tn) : -1;
+    while (tok < total) {
+        // ahead: the next token's record and the position of the token after it
+        long long tnn = tn + nw;
+        int t_nn = -1;
+        GRec rn = rc;
+        if constexpr (kPersistent<RefT>) {
+            t_nn = tnn < total ? __ldg(sel + tnn) : -1;
+            rn = load_rec(lane, t_n, tn < total && t_n >= 0 && t_n < T,
+                          (size_t)(tn < total ? tn / n_sel : 0) * T + t_n, d_c, bits, codes, hdr, ref_idx);
+            asm volatile("" ::: "memory");
+        } else {
+            tn = total;                                 // one token per warp
         }
-    }
-    if (!ok) {
-        for (int c = lane * 8; c < d_c; c += 256) store8(oz + c, zero8);
-        for (int c = lane * 8; c < W; c += 256) store8(om + c, zero8);
-        return;
-    }
 
-    // z~: each lane decodes 8 coordinates per step
-    for (int c = lane * 8; c < d_c; c += 256) {
-        float2 h = h0;
-        uint32_t word = word0;
-        if (c >= 256) {
-            h = __ldg(hrow + (c >> 5));
-            word = bits == 4 ? __ldg((const uint32_t *)(crow + (c >> 1)))
-                             : (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
-        }
-        float v[8];
+        // ---- the current token
+        const int lb = (int)(tok / n_sel);
+        OutT *oz = out_z + (size_t)tok * d_c;
+        OutT *om = out_mean + (size_t)tok * W;
+        bool ok = t >= 0 && t < T;
+        if (t >= T) set_status(status, RKV_ERR_INDEX);
+        const int slots[4] = {rc.ix.x, rc.ix.y, rc.ix.z, rc.ix.w};
+        int k = 0;
+        if (ok) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t q = bits == 4 ? (word >> (4 * j)) & 15u : (word >> (2 * j)) & 3u;
-            v[j] = fmaf((float)q, h.y, h.x);
+            for (int j = 0; j < 4; ++j) {
+                if (slots[j] >= n_ref) { ok = false; set_status(status, RKV_ERR_INDEX); }
+                if (slots[j] >= 0) ++k;
+            }
         }
-        store8(oz + c, v);
-    }
+        if (!ok) {
+            for (int c = lane * 8; c < d_c; c += 256) store8(oz + c, zero8);
+            for (int c = lane * 8; c < W; c += 256) store8(om + c, zero8);
+        } else {
+            // z~: each lane decodes 8 coordinates per step
+            const size_t rec = (size_t)lb * T + t;
+            int u = 0;
+            for (int c = lane * 8; c < d_c; c += 256, ++u) {
+                float2 h;
+                uint32_t word;
+                if (u < 2) {
+                    h = u == 0 ? rc.h[0] : rc.h[1];
+                    word = u == 0 ? rc.w[0] : rc.w[1];
+                } else {
+                    const uint8_t *crow = codes + rec * (size_t)(d_c * bits / 8);
+                    h = __ldg(hdr + rec * (size_t)(d_c / 32) + (c >> 5));
+                    word = bits == 4 ? __ldg((const uint32_t *)(crow + (c >> 1)))
+                                     : (uint32_t)__ldg((const uint16_t *)(crow + (c >> 2)));
+                }
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t q = bits == 4 ? (word >> (4 * j)) & 15u : (word >> (2 * j)) & 3u;
+                    v[j] = fmaf((float)q, h.y, h.x);
+                }
+                store8(oz + c, v);
+            }
 
-    // mean of the stored references, summed in ascending slot order, times 1/k
-    const RefT *rbase = ref_vec + (size_t)lb * n_ref * W;
-    const float inv_k = k > 0 ? 1.0f / (float)k : 0.0f;
-    const float2 ik2 = make_float2(inv_k, inv_k);
-#pragma unroll 4
-    for (int c = lane * 8; c < W; c += 256) {
-        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // mean of the stored references, summed in ascending slot order, times 1/k
+            const RefT *rbase = ref_vec + (size_t)lb * n_ref * W;
+            const float inv_k = k > 0 ? 1.0f / (float)k : 0.0f;
+            const float2 ik2 = make_float2(inv_k, inv_k);
+#pragma unroll (kPersistent<RefT> ? 2 : 4)
+            for (int c = lane * 8; c < W; c += 256) {
+                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a);
+                for (int j = 0; j < 4; ++j)
+                    if (slots[j] >= 0) RefLoad<RefT>::add(rbase + (size_t)slots[j] * W + c, a);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 m = __fmul2_rn(make_float2(a[2 * j], a[2 * j + 1]), ik2);
-            a[2 * j] = m.x;
-            a[2 * j + 1] = m.y;
+                for (int j = 0; j < 4; ++j) {
+                    const float2 m = __fmul2_rn(make_float2(a[2 * j], a[2 * j + 1]), ik2);
+                    a[2 * j] = m.x;
+                    a[2 * j + 1] = m.y;
+                }
+                store8(om + c, a);
+            }
         }
-        store8(om + c, a);
+        tok = tn;
+        t = t_n;
+        rc = rn;
+        tn = tnn;
+        t_n = t_nn;
     }
 }
 
@@ -176,7 +235,9 @@ static void gather_out(const Geometry &g, const rkv_ref_pool *pool, const rkv_ca
                        int32_t *status, cudaStream_t s)
 {
     long long total = (long long)g.LB * n_sel;
-    unsigned blocks = (unsigned)((total * 32 + 255) / 256);
+    // 8-warp blocks: one warp per token, or at most the resident blocks (persistent warps)
+    const long long need = (total + 7) / 8, cap = (long long)kGatherBlocks<RefT> * device_sm_count();
+    unsigned blocks = (unsigned)(kPersistent<RefT> && need > cap ? cap : need);
     ProfScope prof("gather_dequant", s);
     if (out_dtype == RKV_BF16)
         k_gather<RefT, __nv_bfloat16><<<blocks, 256, 0, s>>>(
