@@ -61,10 +61,18 @@ template <> struct RefLoad<uint8_t> {     // FP8 E4M3: exact in fp16, two per co
         const uint2 raw = *(const uint2 *)p;
         const uint32_t w[2] = {raw.x, raw.y};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[j >> 1] >> (16 * (j & 1))) & 0xffffu);
-            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-            add_f16x2((uint32_t)h2.x | ((uint32_t)h2.y << 16), a[2 * j], a[2 * j + 1]);
+        for (int j = 0; j < 2; ++j) {
+            // a word's four bytes: its two 16-bit halves converted to fp16 pairs, then four
+            // widening adds
+            float *aj = a + 4 * j;
+            asm("{\n\t.reg .b16 b0, b1;\n\t.reg .b32 p0, p1;\n\t.reg .f16 f0, f1, f2, f3;\n\t"
+                "mov.b32 {b0, b1}, %4;\n\t"
+                "cvt.rn.f16x2.e4m3x2 p0, b0;\n\tcvt.rn.f16x2.e4m3x2 p1, b1;\n\t"
+                "mov.b32 {f0, f1}, p0;\n\tmov.b32 {f2, f3}, p1;\n\t"
+                "add.rn.f32.f16 %0, f0, %0;\n\tadd.rn.f32.f16 %1, f1, %1;\n\t"
+                "add.rn.f32.f16 %2, f2, %2;\n\tadd.rn.f32.f16 %3, f3, %3;\n\t}"
+                : "+f"(aj[0]), "+f"(aj[1]), "+f"(aj[2]), "+f"(aj[3])
+                : "r"(w[j]));
         }
     }
 };
