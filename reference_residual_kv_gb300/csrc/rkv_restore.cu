@@ -163,15 +163,19 @@ template <bool FP8> struct RefChunk {
             for (int v = 0; v < kU; ++v) {
                 const uint32_t wv[4] = {u[q][v].x, u[q][v].y, u[q][v].z, u[q][v].w};
                 if (FP8) {
+                    // a word's four E4M3 bytes: its two 16-bit halves converted to fp16
+                    // pairs, then four widening adds (byte i into accumulator i)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-                        const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-                        const uint32_t hw = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
-                        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-                            "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
-                            : "+f"(m[v * 16 + 2 * e]), "+f"(m[v * 16 + 2 * e + 1])
-                            : "r"(hw));
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        float *mm = m + v * 16 + 4 * w4;
+                        asm("{\n\t.reg .b16 b0, b1;\n\t.reg .b32 p0, p1;\n\t.reg .f16 f0, f1, f2, f3;\n\t"
+                            "mov.b32 {b0, b1}, %4;\n\t"
+                            "cvt.rn.f16x2.e4m3x2 p0, b0;\n\tcvt.rn.f16x2.e4m3x2 p1, b1;\n\t"
+                            "mov.b32 {f0, f1}, p0;\n\tmov.b32 {f2, f3}, p1;\n\t"
+                            "add.rn.f32.f16 %0, f0, %0;\n\tadd.rn.f32.f16 %1, f1, %1;\n\t"
+                            "add.rn.f32.f16 %2, f2, %2;\n\tadd.rn.f32.f16 %3, f3, %3;\n\t}"
+                            : "+f"(mm[0]), "+f"(mm[1]), "+f"(mm[2]), "+f"(mm[3])
+                            : "r"(wv[w4]));
                     }
                 } else {
 #pragma unroll
