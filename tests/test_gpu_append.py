@@ -68,3 +68,27 @@ def test_append_rejects_out_of_range_position():
     for t in (-1, cfg.T):
         with pytest.raises(rkv.RkvError):
             bufs.append(x, t, x, x, x)
+
+
+def test_append_full_size_sampled():
+    # the benchmark's decode write: after the batch write of all 32 x 8192 tokens, the
+    # last position of every layer appended in one call; its records equal the batch
+    # write's and match the oracle on sampled layers
+    cfg = C["llama3.1-8b-kv"]
+    kv, w = gen_inputs(cfg)
+    bufs, (kv_d, W1, W2, W3) = run_gpu(cfg, kv, w, want_z=False)
+    before = host_records(cfg, bufs)
+    t = cfg.T - 1
+    LB = cfg.L * cfg.B
+    bufs.codes[:, t] = 0xAB
+    bufs.hdr[:, t] = float("nan")
+    bufs.ref_idx[:, t] = -7
+    bufs.append(kv_d.view(LB, cfg.T, -1)[:, t].contiguous(), t, W1, W2, W3)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == 0
+    after = host_records(cfg, bufs)
+    assert np.array_equal(after["idx"][:, t], before["idx"][:, t])
+    report = {}
+    for l in (0, 13, 31):
+        check_tokens(cfg, kv[l][0], w[l], after, l * cfg.B, np.array([t]), report=report)
+    assert report["flips"] <= CODE_BUDGET * report["coords"], report

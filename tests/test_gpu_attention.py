@@ -102,3 +102,21 @@ def test_restore_then_attention_matches_the_oracle_chain():
     want = oracle.attention(wl.stored_to_f64(q[0], "bf16"), K, V, cfg.N)
     got = out.cpu().numpy()[0]
     assert np.abs(got - want).max() <= 1e-2 * np.abs(want).max()
+
+
+def test_attention_full_size():
+    # as the benchmark runs it: 32 query heads on 8 KV heads over one long-context decode
+    # step's whole selection (~39.7 k rows), one call
+    cfg = C["long-131k-fp8ref"]
+    sel = wl.gather_selection(cfg, 0).astype(np.int32)[None]
+    n = sel.shape[1]
+    dk = cfg.N * cfg.D
+    rng = np.random.default_rng(5)
+    K = wl.store(rng.normal(size=(1, n, dk)), "bf16")
+    V = wl.store(rng.normal(size=(1, n, dk)), "bf16")
+    q = wl.decode_queries(cfg, 0, 0)
+    got = _attend(cfg, q, K, V, sel)
+    want = oracle.attention(wl.stored_to_f64(q[0], "bf16"), wl.stored_to_f64(K[0], "bf16"),
+                            wl.stored_to_f64(V[0], "bf16"), cfg.N)
+    scale = np.abs(want).max()
+    assert np.abs(got[0] - want).max() <= 1e-4 * scale, np.abs(got[0] - want).max() / scale

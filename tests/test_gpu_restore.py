@@ -157,3 +157,33 @@ def test_restore_padding_and_out_of_range_indices():
         assert not k[j].any() and not v[j].any()
     for j in (0, 2, 4):                                 # the others are restored
         assert np.abs(v[j]).max() > 0
+
+
+def test_restore_full_size_sampled():
+    # the long-context workload as the benchmark restores it: one decode step's whole
+    # selection (30 % of 131,072 positions plus the last 512) in one call, FP8 pool;
+    # sampled rows against the oracle
+    cfg = C["long-131k-fp8ref"]
+    ensure_lib()
+    p = rkv.params_from_config(cfg)
+    bufs = rkv.Buffers(p)
+    rec = wl.synthetic_records(cfg, bufs.n_ref, 0)
+    load_records(cfg, bufs, [rec])
+    Wd = wl.decoder_weights(cfg, 0)
+    sel = wl.gather_selection(cfg, 0).astype(np.int32)[None]
+    n = sel.shape[1]
+    dk = cfg.N * cfg.D
+    out_k = torch.empty((1, n, dk), dtype=torch.bfloat16, device="cuda")
+    out_v = torch.empty_like(out_k)
+    bufs.restore(to_device(Wd[None], cfg.kv_dtype), torch.from_numpy(sel).cuda(), out_k, out_v,
+                 cfg.rope_base)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == 0
+    pick = np.sort(np.random.default_rng(11).choice(n, 64, replace=False))
+    pick[-1] = n - 1                                     # the last position
+    q, zmin, delta, idx, refs = rec
+    K, V = oracle.restore(cfg, refs_f64(cfg, refs), q, zmin, delta, idx,
+                          wl.stored_to_f64(Wd, cfg.kv_dtype), sel[0][pick])
+    idx_t = torch.from_numpy(pick).cuda()
+    compare_rows(out_k[0].index_select(0, idx_t).float().cpu().numpy(), K, "full-size keys")
+    compare_rows(out_v[0].index_select(0, idx_t).float().cpu().numpy(), V, "full-size values")
