@@ -99,6 +99,8 @@ int device_sm_count();
 // (rkv_umma.cu); false if the driver rejects it.
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
               uint64_t batch, uint32_t box_rows);
+bool make_map_store(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t batch,
+                    uint32_t box_inner, uint32_t box_rows);
 
 // single-token write (rkv_pool.cu: the pool entry; rkv_append.cu: the record)
 cudaError_t launch_append_ref(const Geometry &g, const void *kv_new, int t, const rkv_ref_pool *pool,

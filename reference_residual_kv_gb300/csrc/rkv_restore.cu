@@ -32,8 +32,13 @@ constexpr int kThr = 64 + 32 * kEpi;
 constexpr int kMaxDc = 512;                    // resident z~ tile: 128 rows x d_c bf16
 constexpr int kZBytes = kBM * kMaxDc * 2;      // 128 KB
 constexpr int kWBytes = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 W_d rows x 64
-constexpr int kStages = 5;
-constexpr int kSmem = kZBytes + kStages * kWBytes + 1024 + 256;
+constexpr int kStages = 4;
+// output staging: per epilogue warp two 32-row x 32-column bf16 tiles (64-byte swizzle),
+// each written back by one TMA store
+constexpr int kOutTile = 32 * 32 * 2;
+constexpr int kOutBytes = kEpi * 2 * kOutTile;
+constexpr int kSmem = kZBytes + kStages * kWBytes + kOutBytes + 1024 + 256;
+static_assert(kSmem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
 constexpr int kMaxPairs = 128;                 // D <= 256
 
 struct RestoreArgs {
@@ -47,29 +52,19 @@ struct RestoreArgs {
     const void *ref_vec;
     __nv_bfloat16 *out_k, *out_v;
     int32_t *status;
-    float2 theta[kMaxPairs];                   // base^(-2i/D) as hi + lo floats
+    uint32_t turns[kMaxPairs];                 // theta_i / (2 pi) as a 0.32 fixed-point fraction
 };
 
-// 2 pi = k2PiA + k2PiB + k2PiC (k2PiA has 8 significant bits, so kq * k2PiA is exact
-// for |kq| < 2^15, and the first reduction step is exact)
-constexpr float k2PiA = 6.28125f;
-constexpr float k2PiB = (float)(6.283185307179586476925 - 6.28125);
-constexpr float k2PiC = (float)(6.283185307179586476925 - 6.28125 - (double)(float)(6.283185307179586476925 - 6.28125));
-constexpr float kInv2Pi = 0.15915494309189533577f;
-
-// cos and sin of pos * theta, theta = hi + lo: the product is formed as a two-float sum
-// (the rounding error of pos * hi recovered with an fma), reduced modulo 2 pi with a
-// three-part 2 pi (Cody-Waite), then evaluated on |r| <= ~pi.
-__device__ __forceinline__ void rope_cs(float pos, float2 th, float &c, float &s)
+// cos and sin of pos * theta_i.  theta_i / (2 pi) is held as a 32-bit fixed-point
+// fraction f_i (theta_i < 2 pi, so no integer part); pos * f_i mod 2^32, one integer
+// multiply, is the angle's fraction of a turn, exact for that f_i.  Read as a signed
+// 32-bit value it lies in [-1/2, 1/2) turns, so the sine and cosine are evaluated on
+// [-pi, pi).  Rounding f_i to 32 bits moves the angle by at most pos * 2^-33 turns
+// (1e-4 rad at pos = 2^17), far below the bf16 rounding of the output.
+__device__ __forceinline__ void rope_cs(uint32_t pos, uint32_t f, float &c, float &s)
 {
-    const float a_hi = pos * th.x;
-    const float a_lo = fmaf(pos, th.y, fmaf(pos, th.x, -a_hi));
-    const float kq = rintf(a_hi * kInv2Pi);
-    float r = fmaf(-kq, k2PiA, a_hi);
-    r = fmaf(-kq, k2PiB, r);
-    r = fmaf(-kq, k2PiC, r);
-    r += a_lo;
-    __sincosf(r, &s, &c);
+    const int32_t frac = (int32_t)(pos * f);
+    __sincosf((float)frac * 1.4629180792671596e-09f, &s, &c);   // 2 pi / 2^32
 }
 
 // One lane's share of a token row of z~: coordinates [lane*cpl, (lane+1)*cpl),
@@ -192,12 +187,14 @@ template <bool FP8> struct RefChunk {
 
 template <bool FP8>
 __global__ void __launch_bounds__(kThr, 1)
-k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ RestoreArgs a)
+k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmK,
+          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ RestoreArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *zt = smem_raw + ((1024u - (um::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *wst = zt + kZBytes;                                  // W_d stages
-    uint64_t *full = (uint64_t *)(wst + kStages * kWBytes);       // leader's: both CTAs' bytes
+    uint8_t *ostg = wst + kStages * kWBytes;                      // output tiles
+    uint64_t *full = (uint64_t *)(ostg + kOutBytes);              // leader's: both CTAs' bytes
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;                                  // leader's: both epilogues
@@ -318,7 +315,7 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
         const int row = q * 32 + lane;                      // TMEM lane = z~ row
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t zready_l = um::smem_u32(zready);
-        uint32_t cnt = 0;
+        uint32_t cnt = 0, sb = 0;
         bool ok = true;
         for (int i = pid; i < n_items; i += npairs) {
             const int lb = i / a.n_groups / a.tiles_t, t = (i / a.n_groups) % a.tiles_t;
@@ -367,8 +364,7 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                 }
             }
             const float inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
-            const float pos = (float)(okt ? tok : 0);
-            const size_t orow = (size_t)lb * a.n_sel + e;
+            const uint32_t pos = (uint32_t)(okt ? tok : 0);
             // (3) the N tiles' accumulators; the next chunk's reference values are
             // loaded while this chunk is rotated and stored
             RefChunk<FP8> rch;
@@ -401,16 +397,14 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
                     const int g1 = n * 4 + cc + 1;
                     if (okt && g1 < ne * 4)
                         rch.load(a, slot, lb, (g1 >> 2) * kBN + h * (kBN / 2) + (g1 & 3) * 32);
-                    if (e >= a.n_sel) continue;
                     const bool is_k = c0 < a.dk;
-                    __nv_bfloat16 *dst = (is_k ? a.out_k + orow * a.dk + c0 : a.out_v + orow * a.dk + (c0 - a.dk));
                     if (okt) {
                         if (is_k) {
                             const int p0 = (c0 % a.D) >> 1;           // first pair index
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 float cs, sn;
-                                rope_cs(pos, a.theta[p0 + j], cs, sn);
+                                rope_cs(pos, a.turns[p0 + j], cs, sn);
                                 const float x0 = o[2 * j], x1 = o[2 * j + 1];
                                 // (x0 cs - x1 sn, x1 cs + x0 sn)
                                 const float2 r = __ffma2_rn(make_float2(-x1, x0), make_float2(sn, sn),
@@ -423,14 +417,28 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
 #pragma unroll
                         for (int j = 0; j < 32; ++j) o[j] = 0.0f;
                     }
+                    // the warp's 32 rows x 32 columns go through shared memory to one TMA
+                    // store (rows past the selection are clipped by the tensor map); a
+                    // staging buffer is rewritten once the store before the last has read it
+                    uint8_t *stg = ostg + ((warp - 2) * 2 + sb) * kOutTile;
+                    if (lane == 0) um::bulk_wait_read<1>();
+                    __syncwarp();
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             pk[j] = __float22bfloat162_rn(make_float2(o[8 * u + 2 * j], o[8 * u + 2 * j + 1]));
-                        *(uint4 *)(dst + 8 * u) = *(const uint4 *)pk;
+                        // 64-byte swizzle: 16-byte unit u of row r at u ^ ((r / 2) % 4)
+                        *(uint4 *)(stg + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) = *(const uint4 *)pk;
                     }
+                    um::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        um::tma_store_3d(is_k ? &tmK : &tmV, stg, is_k ? c0 : c0 - a.dk, e0 + q * 32, lb);
+                        um::bulk_commit();
+                    }
+                    sb ^= 1u;
                 }
                 um::tc_fence_before();
                 __syncwarp();
@@ -442,6 +450,9 @@ k_restore(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Resto
             }
             if (!ok) break;
         }
+        // the warp's stores complete before the CTA leaves
+        if (lane == 0) um::bulk_wait_all();
+        __syncwarp();
         if (!ok) {
             set_status(a.status, RKV_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
@@ -476,12 +487,12 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     a.ref_idx = (const int4 *)cache->ref_idx; a.ref_vec = pool->ref_vec;
     a.out_k = (__nv_bfloat16 *)out_k; a.out_v = (__nv_bfloat16 *)out_v; a.status = status;
     for (int i = 0; i < a.D / 2; ++i) {
+        // the fraction of a turn of theta_i (whole turns do not move the angle)
         const double th = pow(rope_base, -2.0 * (double)i / (double)a.D);
-        const float hi = (float)th;
-        a.theta[i] = make_float2(hi, (float)(th - (double)hi));
+        double f = th / (2.0 * 3.14159265358979323846);
+        f -= floor(f);
+        a.turns[i] = (uint32_t)(llrint(f * 4294967296.0) & 0xffffffffLL);
     }
-    CUtensorMap mW;
-    if (!make_map(&mW, Wd, g.d_c, g.W, g.L, kBN / 2)) return cudaErrorInvalidValue;
 
     auto kern = a.ref_fp8 ? k_restore<true> : k_restore<false>;
     static bool attr[2] = {false, false};
@@ -491,6 +502,11 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
         attr[a.ref_fp8] = true;
     }
     if ((long long)g.LB * a.tiles_t <= 0) return cudaSuccess;
+    CUtensorMap mW, mK, mV;
+    if (!make_map(&mW, Wd, g.d_c, g.W, g.L, kBN / 2) ||
+        !make_map_store(&mK, out_k, a.dk, n_sel, g.LB, 32, 32) ||
+        !make_map_store(&mV, out_v, a.dk, n_sel, g.LB, 32, 32))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -525,7 +541,7 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     const long long np = items < max_pairs ? items : max_pairs;
     cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
     ProfScope prof("restore_kv", s);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mK, mV, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -642,6 +642,23 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
     return r == CUDA_SUCCESS;
 }
 
+// A bf16 [batch][rows][inner] output tensor for TMA stores of box_inner x box_rows tiles
+// from 64-byte-swizzled shared memory (box_inner * 2 bytes = 64).
+bool make_map_store(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t batch,
+                    uint32_t box_inner, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // W_c1 and W_c2 ([L][d_ff][W] each, i.e. [L*d_ff][W]) seen as one [2][L*d_ff][W] tensor
 // whose matrix stride is the distance between them: box = 64 (inner) x 64 rows x both
 // matrices, i.e. 64 rows of W_c1 followed by the same 64 rows of W_c2.

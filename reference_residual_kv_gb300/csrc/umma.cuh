@@ -330,5 +330,28 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v)
     for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// ---- TMA tile stores (bulk async group) ------------------------------------------
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(m), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every store group this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 }  // namespace um
 }  // namespace rkv
