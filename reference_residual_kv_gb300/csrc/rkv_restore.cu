@@ -45,6 +45,7 @@ struct RestoreArgs {
     int LB, B, T, n_sel, W, dk, D, d_c, bits, n_ref, ref_fp8;
     int tiles_t, n_tiles, k_chunks;
     int n_groups, group_tiles;                 // an item: one token tile x group_tiles N tiles
+    int wide;                                  // the pool is 32-byte aligned: 32-byte loads
     const int32_t *sel;
     const uint8_t *codes;
     const float2 *hdr;
@@ -140,8 +141,19 @@ template <bool FP8> struct RefChunk {
             const size_t row = ((size_t)lb * a.n_ref + slot[q]) * a.W + c0;
             const uint4 *p = FP8 ? (const uint4 *)((const uint8_t *)a.ref_vec + row)
                                  : (const uint4 *)((const __nv_bfloat16 *)a.ref_vec + row);
+            if (a.wide) {
+                // 32 bytes per load (one L1 wavefront per row for two 16-byte units)
 #pragma unroll
-            for (int v = 0; v < kU; ++v) u[q][v] = __ldg(p + v);
+                for (int v = 0; v < kU; v += 2)
+                    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                                 : "=r"(u[q][v].x), "=r"(u[q][v].y), "=r"(u[q][v].z), "=r"(u[q][v].w),
+                                   "=r"(u[q][v + 1].x), "=r"(u[q][v + 1].y), "=r"(u[q][v + 1].z),
+                                   "=r"(u[q][v + 1].w)
+                                 : "l"(p + v));
+            } else {
+#pragma unroll
+                for (int v = 0; v < kU; ++v) u[q][v] = __ldg(p + v);
+            }
         }
     }
 
@@ -480,6 +492,8 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     a.ref_fp8 = g.ref_dtype == RKV_FP8_E4M3;
     a.tiles_t = (n_sel + kTileM - 1) / kTileM;
     a.n_tiles = g.W / kBN;
+    // rows and 32-column chunks then start on 32-byte boundaries as well
+    a.wide = ((uintptr_t)pool->ref_vec & 31u) == 0 && ((size_t)g.W * (a.ref_fp8 ? 1 : 2)) % 32 == 0;
     a.n_groups = 1;
     a.group_tiles = a.n_tiles;
     a.k_chunks = g.d_c / kBK;
