@@ -164,11 +164,14 @@ rkv_status rkv_gather_dequant(const rkv_params *p, const rkv_ref_pool *pool,
  * every key head is rotated at the token's own position t (its index in the
  * sequence; the restored key is pre-RoPE [RKV §2.1]): coordinate pairs (2i, 2i+1)
  * by the angle t * rope_base^(-2i/D).  The page does not fix the RoPE variant; this
- * is the rotary embedding as first defined, with consecutive pairs.
+ * is the rotary embedding as first defined, with consecutive pairs.  The angle is
+ * formed in turns, t * (theta_i / 2 pi) mod 1, with theta_i / 2 pi rounded to 32
+ * fractional bits on the host (an angle error below t * 2^-33 turns, 1e-4 rad at
+ * t = 2^17), then evaluated on [-pi, pi).
  * Wd: [L][2 N D][d_c] out-major (Wd[c][j] = W_d[j][c]), bf16.
  * sel: [L*B][n_sel] int32 token positions (-1: padding, zero rows; >= T or a stored
  * slot >= n_ref: RKV_ERR_INDEX in dev_status and zero rows).
- * out_k, out_v: bf16 [L*B][n_sel][N D].
+ * out_k, out_v: bf16 [L*B][n_sel][N D], 16-byte aligned (written by TMA tile stores).
  * The decoder runs on the tensor cores with z~ rounded to bf16 and fp32 accumulation;
  * the mean is an fp32 sum in ascending slot order times 1/k.
  * Requires kv_dtype bf16, d_c in {256, 512}, 2 N D a multiple of 256, D a multiple
