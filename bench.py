@@ -41,7 +41,7 @@ UNIT = "tokens/s"
 # layers by the units processed (its traffic grows in proportion).  Set an entry to None
 # when its kernel changes.
 # layers per chunk of the end-to-end step (copies of one chunk overlap another's compute)
-E2E_CHUNK_LAYERS = 4
+E2E_CHUNK_LAYERS = 2
 
 NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (201.037056e6 + 108.294400e6),
                   "umma_distance_topk": 8 * (174.959360e6 + 6.633728e6)}
@@ -534,7 +534,7 @@ def run_ours(args, cfg):
     # chunk c-2's device->host copy of its records, pool and read outputs.
     e2e = None
     if not args.no_e2e:
-        C = E2E_CHUNK_LAYERS if cfg.L % E2E_CHUNK_LAYERS == 0 else cfg.L
+        C = args.e2e_chunk_layers if cfg.L % args.e2e_chunk_layers == 0 else cfg.L
         nch = cfg.L // C
         pc = rkv.params_from_config(cfg.replace(L=C))
         cbufs = [rkv.Buffers(pc, device=dev) for _ in range(nch)]
@@ -670,6 +670,8 @@ def main():
                     help="run only the long-context sparse-read measurement")
     ap.add_argument("--read-steps", type=int, default=256,
                     help="decode steps of the sparse-read measurement")
+    ap.add_argument("--e2e-chunk-layers", type=int, default=E2E_CHUNK_LAYERS,
+                    help="layers per chunk of the end-to-end step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
