@@ -19,7 +19,7 @@
 namespace rkv {
 namespace {
 
-constexpr int kSlice = 64;        // pool slots per distance CTA
+constexpr int kSlice = 32;        // pool slots per distance CTA
 constexpr int kNoSlot = 0x7fffffff;
 
 struct AppWs {                    // workspace carve-up (floats / ints)
@@ -115,8 +115,6 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
              const float2 *__restrict__ part, int4 *__restrict__ ref_idx, float *__restrict__ mean,
              int *__restrict__ state)
 {
-    constexpr int kStage = 1024;  // slice entries staged in shared memory per round
-    __shared__ float2 pe[kStage];
     __shared__ int ch[kMaxK];
     __shared__ int info[2];       // k_t, state
     const int lb = blockIdx.x;
@@ -125,17 +123,28 @@ k_app_select(int t, int k, const int32_t *__restrict__ ref_slot, const int32_t *
     int fs[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) { fe[j] = INFINITY; fs[j] = kNoSlot; }
-    if (own < 0) {
-        // the slices' candidates: all threads stage them, thread 0 merges them in order
+    if (own < 0 && threadIdx.x < 32) {
+        // the slices' candidates, merged by the first warp: lane l keeps the k best of
+        // entries l, l + 32, ..., then five butterfly rounds merge the lanes' lists
+        // ((distance, slot) is a total order, so the k best are those of a serial merge)
+        const int lane = threadIdx.x;
         const int total = ((pool_size[t] + kSlice - 1) / kSlice) * kMaxK;
         const float2 *src = part + (size_t)lb * slices * kMaxK;
-        for (int base = 0; base < total; base += kStage) {
-            const int cnt = min(kStage, total - base);
-            __syncthreads();
-            for (int i = threadIdx.x; i < cnt; i += blockDim.x) pe[i] = src[base + i];
-            __syncthreads();
-            if (threadIdx.x == 0)
-                for (int i = 0; i < cnt; ++i) list_insert<kMaxK>(fe, fs, pe[i].x, __float_as_int(pe[i].y));
+        for (int i = lane; i < total; i += 32) {
+            const float2 e = src[i];
+            list_insert<kMaxK>(fe, fs, e.x, __float_as_int(e.y));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float pe[kMaxK];
+            int ps[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                pe[j] = __shfl_xor_sync(0xffffffffu, fe[j], o);
+                ps[j] = __shfl_xor_sync(0xffffffffu, fs[j], o);
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) list_insert<kMaxK>(fe, fs, pe[j], ps[j]);
         }
     }
     if (threadIdx.x == 0) {
