@@ -289,7 +289,8 @@ def synthetic_records(cfg: Config, n_ref: int, lb: int = 0):
     """Arbitrary well-formed cache records of one (layer, sequence), for testing the read
     side on its own: codes [T][d_c] uniform in [0, 2^bits), group minima ~ N(0, 0.1^2),
     steps ~ U(0, 0.05) with every 7th group constant (step 0), reference relations of
-    1..k distinct slots in [0, n_ref), ascending, -1 padded; and n_ref pool vectors
+    1..k distinct slots in [0, n_ref) (the first ones of a Floyd sample of k distinct
+    slots), ascending, -1 padded; and n_ref pool vectors
     ~ N(0, 1) stored in ref_dtype (FP8: uniform non-NaN bytes).
     Returns (codes, zmin, delta, ref_idx, refs)."""
     T, C, G, k = cfg.T, cfg.d_c, cfg.d_c // cfg.group, cfg.k
@@ -300,10 +301,20 @@ def synthetic_records(cfg: Config, n_ref: int, lb: int = 0):
     delta = (uniform(key(2), T * G) * 0.05).reshape(T, G)
     delta[:, ::7] = 0.0
     cnt = 1 + np.minimum(np.floor(uniform(key(3), T) * k), k - 1).astype(np.int64)
-    order = np.argsort(uniform(key(4), T * n_ref).reshape(T, n_ref), axis=1, kind="stable")
-    ref_idx = np.full((T, k), -1, np.int32)
-    for t in range(T):
-        ref_idx[t, :cnt[t]] = np.sort(order[t, :cnt[t]])
+    # Floyd's sampling of k distinct slots per row: draw i picks r in [0, j], j = n_ref - k + i,
+    # and takes j instead when r was already taken
+    assert n_ref >= k
+    u = uniform(key(4), T * k).reshape(T, k)
+    first = np.empty((T, k), np.int64)
+    for i in range(k):
+        j = n_ref - k + i
+        r = np.minimum(np.floor(u[:, i] * (j + 1)), j).astype(np.int64)
+        dup = (first[:, :i] == r[:, None]).any(axis=1)
+        first[:, i] = np.where(dup, j, r)
+    # row t: its first cnt[t] sampled slots in ascending order, then -1
+    used = np.arange(k)[None, :] < cnt[:, None]
+    first = np.sort(np.where(used, first, np.iinfo(np.int64).max), axis=1)
+    ref_idx = np.where(first == np.iinfo(np.int64).max, -1, first).astype(np.int32)
     if cfg.ref_dtype == "fp8":
         # stored FP8 bytes drawn directly: any byte but the two NaN codes 0x7f, 0xff
         b = np.floor(uniform(key(5), n_ref * cfg.W) * 254).astype(np.int64)
