@@ -73,19 +73,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
-// Multicast tile load: the box lands at the same shared-memory offset in every CTA of
-// the cluster named in `mask`, and each of them gets the complete_tx on its own
-// mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
-                                               int x, int y, int z, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
 // ---- clusters ------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank()
 {
