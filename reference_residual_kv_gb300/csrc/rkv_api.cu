@@ -127,6 +127,12 @@ static rkv_status check_cache(const rkv_cache *c)
     return RKV_OK;
 }
 
+int current_device()
+{
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 int device_sm_count()
 {
     int dev = 0, n = 0;

@@ -12,6 +12,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <mutex>
+
 #include "../../include/rkv.h"
 
 namespace rkv {
@@ -91,9 +93,34 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
                                  const float2 *cand, const float *xnorm, const float *rn_max,
                                  int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
                                  int32_t *scan_count, int32_t *status, cudaStream_t s);
-// ||x||^2 of every token row (bf16 kv)
 
 int device_sm_count();
+
+// ---- per-device host state ----------------------------------------------------
+// Launch facts that belong to a device (a kernel's raised shared-memory limit, its
+// cluster occupancy, the address of a __device__ array) are set up once per device,
+// on the first call that reaches it, under std::call_once: several host threads and
+// several devices in one process each get their own.
+constexpr int kMaxDevices = 64;
+int current_device();   // the calling thread's current device; -1 on error
+
+template <class T>
+struct PerDevice {
+    std::once_flag once[kMaxDevices];
+    cudaError_t err[kMaxDevices];
+    T value[kMaxDevices];
+};
+
+// Runs setup(value&) once for the current device; returns its error and the value.
+template <class T, class F>
+cudaError_t per_device(PerDevice<T> &pd, T &value, F setup)
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(pd.once[dev], [&] { pd.err[dev] = setup(pd.value[dev]); });
+    value = pd.value[dev];
+    return pd.err[dev];
+}
 
 // bf16 [batch][rows][inner] tensor map, box = 64 (inner) x box_rows, 128-byte swizzle
 // (rkv_umma.cu); false if the driver rejects it.

@@ -16,20 +16,19 @@ namespace rkv {
 constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;   // 64 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array, looked up once per device.  In host code the name
-// g_noalloc_scratch is only a host-side stand-in, not a device address.
-constexpr int kMaxDevices = 64;
-static void *g_scratch_addr[kMaxDevices];
+// Device address of the array, looked up once per device with that device current
+// (thread-safe).  In host code the name g_noalloc_scratch is only a host-side
+// stand-in, not a device address: only the looked-up address may reach a kernel.
+static PerDevice<void *> g_scratch;
 
-static void *scratch_address(int dev)
+static cudaError_t scratch_address(void *&ptr)
 {
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    return per_device(g_scratch, ptr, [](void *&p) {
+        p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e == cudaSuccess && p == nullptr) e = cudaErrorInvalidSymbol;
+        return e;
+    });
 }
 
 }  // namespace rkv
@@ -46,10 +45,8 @@ extern "C" rkv_status rkv_compress_noalloc(const rkv_params *p, const void *kv,
     rkv_status st = rkv_query_sizes(p, nullptr, nullptr, &need);
     if (st != RKV_OK) return st;
     if (need > kNoAllocScratchBytes) return RKV_ERR_WORKSPACE;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RKV_ERR_CUDA;
-    void *scratch = scratch_address(dev);
-    if (!scratch) return RKV_ERR_CUDA;
+    void *scratch = nullptr;
+    if (scratch_address(scratch) != cudaSuccess || !scratch) return RKV_ERR_CUDA;
     return rkv_compress(p, kv, pool, W1t, W2t, W3t, cache, scratch, kNoAllocScratchBytes, z_out,
                         dev_status, stream);
 }

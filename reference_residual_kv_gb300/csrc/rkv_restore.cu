@@ -509,12 +509,6 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     }
 
     auto kern = a.ref_fp8 ? k_restore<true> : k_restore<false>;
-    static bool attr[2] = {false, false};
-    if (!attr[a.ref_fp8]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        attr[a.ref_fp8] = true;
-    }
     if ((long long)g.LB * a.tiles_t <= 0) return cudaSuccess;
     CUtensorMap mW, mK, mV;
     if (!make_map(&mW, Wd, g.d_c, g.W, g.L, kBN / 2) ||
@@ -532,12 +526,24 @@ cudaError_t launch_restore(const Geometry &g, const rkv_ref_pool *pool, const rk
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    static int max_pairs = 0;
-    if (max_pairs == 0) {
-        cfg.gridDim = dim3(2 * 64, 1, 1);
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)kern, &cfg);
-        if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
-    }
+    // per device and reference type: the raised shared-memory limit, then the pairs
+    // that fit at once
+    static PerDevice<int> setup[2];
+    int max_pairs = 0;
+    cudaError_t se = per_device(setup[a.ref_fp8 ? 1 : 0], max_pairs, [&](int &mp) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * 64, 1, 1);
+        mp = 0;
+        e = cudaOccupancyMaxActiveClusters(&mp, (void *)kern, &q);
+        if (e != cudaSuccess || mp <= 0) {
+            (void)cudaGetLastError();
+            mp = device_sm_count() / 2;
+        }
+        return cudaSuccess;
+    });
+    if (se != cudaSuccess) return se;
     // N-tile groups: the split whose rounds of items over the pairs, each costing its
     // tiles plus about half a tile for writing the z~ tile, finish first
     {
