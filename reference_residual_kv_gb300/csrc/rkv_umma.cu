@@ -97,6 +97,17 @@ __device__ __forceinline__ int item_count(const UmmaArgs &a)
     return a.LB * a.tiles_t * a.tiles_n;
 }
 
+// Work item of pair `pid` in round r.  A round takes the next npairs items of the
+// order; odd rounds hand them out in reverse (boustrophedon), so that where item
+// costs fall along the order (distance items: late token tiles first, and a tile's
+// later reference chunks are shorter) every pair's total evens out.  Dealing items
+// out with a fixed stride instead gave each pair the same chunk index of every tile
+// whenever the number of pairs is a multiple of the chunk count.
+__device__ __forceinline__ int item_at(int r, int pid, int npairs)
+{
+    return r * npairs + ((r & 1) ? npairs - 1 - pid : pid);
+}
+
 // The (layer, sequence) index is the slowest, so the pairs in flight share one layer's
 // weights, references and projections in L2; the N index is the fastest, so
 // neighbouring pairs reuse the same token rows.  Distance items visit the late
@@ -199,7 +210,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             bool used[S];
             for (int s = 0; s < S; ++s) { used[s] = false; last_ph[s] = 0; }
             bool ok = true;
-            for (int i = pid; i < n_items && ok; i += npairs) {
+            for (int rnd = 0; rnd * npairs < n_items && ok; ++rnd) {
+                const int i = item_at(rnd, pid, npairs);
+                if (i >= n_items) continue;
                 Item it;
                 if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
@@ -256,7 +269,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             int stage = 0;
             uint32_t ph = 0, cnt = 0;
             bool ok = true;
-            for (int i = pid; i < n_items && ok; i += npairs) {
+            for (int rnd = 0; rnd * npairs < n_items && ok; ++rnd) {
+                const int i = item_at(rnd, pid, npairs);
+                if (i >= n_items) continue;
                 Item it;
                 if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
@@ -312,7 +327,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int stage = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int i = pid; i < n_items && ok; i += npairs) {
+        for (int rnd = 0; rnd * npairs < n_items && ok; ++rnd) {
+            const int i = item_at(rnd, pid, npairs);
+            if (i >= n_items) continue;
             Item it;
             if (!item_get<MODE>(a, i, it)) continue;
             for (int n = it.n0; n < it.n1 && ok; ++n) {
@@ -360,7 +377,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         const int pair_id = 1 + (q & 1) + 2 * h;
         uint32_t cnt = 0, xcnt = 0;
         bool ok = true;
-        for (int i = pid; i < n_items; i += npairs) {
+        for (int rnd = 0; rnd * npairs < n_items; ++rnd) {
+            const int i = item_at(rnd, pid, npairs);
+            if (i >= n_items) continue;
             Item it;
             if (!item_get<MODE>(a, i, it)) continue;
             const int r = it.t * 2 * kBM + (int)rank * kBM + row;   // token row (M_DIST, M_S2)
@@ -683,12 +702,6 @@ static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUten
 {
     auto kern = k_umma<MODE>;
     constexpr int smem = Cfg<MODE>::kSmem;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
     const long long items = (long long)args.LB * args.tiles_t * args.tiles_n;
     if (items <= 0) return cudaSuccess;
 
@@ -703,12 +716,23 @@ static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUten
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    static int max_pairs = 0;
-    if (max_pairs == 0) {
-        cfg.gridDim = dim3(2 * 64, 1, 1);
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, (void *)kern, &cfg);
-        if (e != cudaSuccess || max_pairs <= 0) max_pairs = device_sm_count() / 2;
-    }
+    // per device: the raised shared-memory limit, then the pairs that fit at once
+    static PerDevice<int> setup;
+    int max_pairs = 0;
+    cudaError_t se = per_device(setup, max_pairs, [&](int &mp) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * 64, 1, 1);
+        mp = 0;
+        e = cudaOccupancyMaxActiveClusters(&mp, (void *)kern, &q);
+        if (e != cudaSuccess || mp <= 0) {
+            (void)cudaGetLastError();
+            mp = device_sm_count() / 2;
+        }
+        return cudaSuccess;
+    });
+    if (se != cudaSuccess) return se;
     const long long np = items < max_pairs ? items : max_pairs;
     cfg.gridDim = dim3((unsigned)(2 * np), 1, 1);
     static const char *names[4] = {"umma_ref_proj", "umma_distance_topk", "umma_swiglu_diff",
