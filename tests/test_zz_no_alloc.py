@@ -1,8 +1,9 @@
 """rkv_compress_noalloc, the entry point for callers that cannot allocate device
 memory at the call (graph capture, foreign arenas, allocation-free serving loops):
-it must produce what rkv_compress produces with a caller workspace, on two calls in a
-row (its built-in scratch keeps the previous call's bytes), and refuse problems whose
-scratch would not fit.  Kept in a file pytest collects last."""
+it must produce exactly what rkv_compress produces with a caller workspace (records
+and z bit for bit), on two calls in a row (its built-in scratch keeps the previous
+call's bytes), and refuse problems whose scratch would not fit.  Kept in a file
+pytest collects last."""
 import numpy as np
 import pytest
 import torch
@@ -11,8 +12,6 @@ import rkv_workload as wl
 from reference_residual_kv_gb300 import build, rkv
 
 pytestmark = pytest.mark.gpu
-
-Z_TOL = 2e-2
 
 
 def _dev(a, dtype):
@@ -46,19 +45,18 @@ def test_noalloc_matches_workspace_entry_point(cfg):
         out = rkv.Buffers(p, want_z=True)
         out.build_ref_pool(kv)
         out.codes.fill_(0xAB)
+        out.hdr.fill_(float("nan"))
+        out.ref_idx.fill_(-7)
         out.z.fill_(float("nan"))
         rkv.rkv_compress_noalloc(p, kv, out.pool, W1, W2, W3, out.cache, out.z, out.status)
         torch.cuda.synchronize()
         assert out.device_status() == 0 and ref.device_status() == 0
+        # the same kernels on the same inputs: every record bit for bit (the kernels
+        # are deterministic; only where the scratch lives differs)
         assert torch.equal(out.ref_idx, ref.ref_idx)
-        zr, zo = ref.z.cpu().numpy(), out.z.cpu().numpy()
-        scale = np.maximum(np.abs(zr).max(axis=-1, keepdims=True), 1e-3 * np.abs(zr).max())
-        assert np.all(np.abs(zo - zr) <= Z_TOL * scale)
-        qr = ref.codes.cpu().numpy()
-        qo = out.codes.cpu().numpy()
-        assert (qr != qo).mean() <= 1e-3
-        np.testing.assert_allclose(out.hdr.cpu().numpy(), ref.hdr.cpu().numpy(),
-                                   rtol=0, atol=float(Z_TOL * scale.max()))
+        assert torch.equal(out.codes, ref.codes)
+        assert torch.equal(out.hdr.view(torch.int32), ref.hdr.view(torch.int32))
+        assert torch.equal(out.z.view(torch.int32), ref.z.view(torch.int32))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
