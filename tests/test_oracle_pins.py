@@ -34,11 +34,25 @@ def test_fixed_schedule_positions():
 
 
 def test_dynamic_schedule_table6_counts():
-    # Table VI reference counts at 262K for five alphas (all five reproduced exactly
-    # under the stated reading); catches a wrong floor argument or recurrence sign.
+    # Table VI reference counts at 262K for five alphas, all five reproduced exactly
+    # under the fitted reading (262144 - 256 positions); catches a wrong floor
+    # argument or recurrence sign.
     g = _golden("table6_ref_counts.json")
     got = [oracle.dynamic_schedule(g["T"], g["s0"], a, g["n_sink"]).size for a in g["alpha"]]
     assert got == g["n_ref"]
+
+
+def test_dynamic_schedule_table6_unfitted_reading():
+    # Table VI [RKV §4.6] over the whole 262144-position context with no positions
+    # dropped: every alpha > 0 count is within 1 of the table, and alpha = 0 gives the
+    # fixed-stride count ceil(T / s0) (the table prints 26 fewer; only the fitted
+    # reading above matches it exactly)
+    g = _golden("table6_ref_counts.json")
+    T = g["unfitted_T"]
+    got = [oracle.dynamic_schedule(T, g["s0"], a, g["n_sink"]).size for a in g["alpha"]]
+    assert got[0] == -(-T // g["s0"])
+    for n, ref in zip(got[1:], g["n_ref"][1:]):
+        assert abs(n - ref) <= 1, (got, g["n_ref"])
 
 
 def test_dynamic_schedule_alpha0_is_fixed_and_log_growth():
