@@ -246,6 +246,18 @@ rkv_status rkv_profile_enable(int32_t on);
 int32_t rkv_profile_collect(char *names, int32_t name_len, float *total_ms, int32_t *launches,
                             int32_t max_entries);
 
+/* Test hook of the device-side timeout path (failure handling; the paper has no
+ * counterpart).  Arms a one-shot fault that the next rkv_compress call with bf16 kv,
+ * from any host thread, takes in its W_c3 kernel: every barrier wait of that kernel
+ * gives up after wait_cycles SM clock cycles instead of about 2e9, and the second CTA
+ * of every CTA pair skips its tile loads for its stage use number skip_use, so that a
+ * wait runs out.  The kernel then sets RKV_ERR_DEVICE_TIMEOUT in *dev_status, lets the
+ * copies and MMAs it issued finish, frees its tensor memory and returns: nothing
+ * traps, and the context stays usable for later calls.  The records of that call are
+ * incomplete.  For tests of the error path only.  Returns RKV_ERR_INVALID_ARG unless
+ * 1e4 <= wait_cycles <= 2e9 and skip_use >= 0.                                      */
+rkv_status rkv_debug_wait_fault(int64_t wait_cycles, int32_t skip_use);
+
 /* Static description of a status code. */
 const char *rkv_status_string(rkv_status s);
 

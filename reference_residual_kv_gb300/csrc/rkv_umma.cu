@@ -38,6 +38,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 namespace rkv {
 
 enum { M_P = 0, M_DIST = 1, M_S1 = 2, M_S2 = 3 };
@@ -87,6 +89,9 @@ struct UmmaArgs {
     int32_t *status;
     const __nv_bfloat16 *xrows;   // M_DIST: the token rows (bf16, [LB*T][W]) ...
     float *xnorm;                 // ... and their ||x||^2, written by the norm warps
+    long long wait_cycles;        // limit of every barrier wait (a.wait_cycles)
+    int skip_use;                 // test hook: the pair peer skips its loads for this
+                                  // stage use (-1: never)
 };
 
 // One work item of a pair: (lb, token tile t of 256 rows, N range [n0, n1)).
@@ -210,6 +215,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             bool used[S];
             for (int s = 0; s < S; ++s) { used[s] = false; last_ph[s] = 0; }
             bool ok = true;
+            int use = 0;
             for (int rnd = 0; rnd * npairs < n_items && ok; ++rnd) {
                 const int i = item_at(rnd, pid, npairs);
                 if (i >= n_items) continue;
@@ -217,10 +223,18 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     for (int kc = 0; kc < k_iters; ++kc) {
-                        const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, kWaitCycles);
+                        const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, a.wait_cycles);
                         if (*abort_flag || !w) {
                             ok = false;
                             break;
+                        }
+                        // test hook of the timeout path: the peer leaves one stage
+                        // short, so the leader's full barrier never completes
+                        if (!leader && use++ == a.skip_use) {
+                            used[stage] = true;
+                            last_ph[stage] = ph;
+                            if (++stage == S) { stage = 0; ph ^= 1u; }
+                            continue;
                         }
                         uint8_t *sa = tiles + stage * kStageBytes;
                         uint8_t *sb = sa + kABytes;
@@ -261,7 +275,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             }
             // a stage's copies have landed once the pair's MMA has freed it
             for (int s = 0; s < S; ++s)
-                if (used[s]) um::mbar_wait(&empty[s], last_ph[s], kWaitCycles);
+                if (used[s]) um::mbar_wait(&empty[s], last_ph[s], a.wait_cycles);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -276,7 +290,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
-                    const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, kWaitCycles);
+                    const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, a.wait_cycles);
                     if (*abort_flag || !w) {
                         ok = false;
                         break;
@@ -286,7 +300,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // distance tiles: only the references the tile's rows can see
                     const uint32_t id = MODE == M_DIST ? um::idesc_bf16_f32(2 * kBM, dist_cols(a, it.t, n)) : kIdesc;
                     for (int kc = 0; kc < k_iters; ++kc) {
-                        const bool wf = um::mbar_wait(&full[stage], ph, kWaitCycles);
+                        const bool wf = um::mbar_wait(&full[stage], ph, a.wait_cycles);
                         if (*abort_flag || !wf) {
                             ok = false;
                             break;
@@ -312,7 +326,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             }
             // all issued MMAs complete before TMEM can be released
             um::mma2_commit_mc(drain, 1);
-            um::mbar_wait(drain, 0, kWaitCycles);
+            um::mbar_wait(drain, 0, a.wait_cycles);
         }
     } else if (MODE == M_DIST && warp >= 2 + kEpiWarps) {
         // ------------------------------------------------------------ token norms
@@ -336,7 +350,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const bool need = it.chunk == 0 && n == 0;
                 float acc = 0.0f;
                 for (int kc = 0; kc < k_iters; ++kc) {
-                    const bool w = um::mbar_wait(leader ? &full[stage] : &landed[stage], ph, kWaitCycles);
+                    const bool w = um::mbar_wait(leader ? &full[stage] : &landed[stage], ph, a.wait_cycles);
                     if (*abort_flag || !w) {
                         ok = false;
                         break;
@@ -434,7 +448,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 
             for (int n = it.n0; n < it.n1; ++n) {
                 const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
-                bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, kWaitCycles);
+                bool w = !*abort_flag && um::mbar_wait(&tfull[buf], tph, a.wait_cycles);
                 w = __all_sync(0xffffffffu, w);
                 if (MODE == M_S1) w = um::bar_and(pair_id, 64, w);   // the pair leaves together
                 if (!w) { ok = false; break; }
@@ -631,6 +645,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 }
 
 // ---------------------------------------------------------------------------- host
+// One-shot fault of the timeout path, armed by rkv_debug_wait_fault and taken by the
+// next W_c3 launch of the write path.
+static std::atomic<long long> g_fault_cycles{0};
+static std::atomic<int> g_fault_skip{-1};
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -762,6 +781,8 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         return e;
 
     UmmaArgs a{};
+    a.wait_cycles = kWaitCycles;
+    a.skip_use = -1;
     a.LB = g.LB; a.B = g.B; a.T = g.T; a.W = g.W; a.d_ff = g.d_ff; a.d_c = g.d_c;
     a.n_ref = g.n_ref; a.bits = g.bits;
     a.P1 = P1; a.P2 = P2; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
@@ -821,9 +842,25 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         UmmaArgs p = a;
         p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = (g.d_c + kBN - 1) / kBN;
         p.k_chunks = (g.d_ff + kBK - 1) / kBK; p.a_sources = 2;
+        const long long fc = g_fault_cycles.exchange(0);
+        const int fs = g_fault_skip.exchange(-1);
+        if (fc > 0 && fs >= 0) {
+            p.wait_cycles = fc;
+            p.skip_use = fs;
+        }
         if ((e = run<M_S2>(mHi, mLo, mW3, p, s)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 }  // namespace rkv
+
+using namespace rkv;
+
+extern "C" rkv_status rkv_debug_wait_fault(int64_t wait_cycles, int32_t skip_use)
+{
+    if (wait_cycles < 10000 || wait_cycles > kWaitCycles || skip_use < 0) return RKV_ERR_INVALID_ARG;
+    g_fault_skip.store(skip_use);
+    g_fault_cycles.store(wait_cycles);
+    return RKV_OK;
+}

@@ -19,7 +19,7 @@ RKV_ERR_CUDA, RKV_ERR_INDEX, RKV_ERR_DEVICE_TIMEOUT, RKV_ERR_WORKSPACE = 4, 5, 6
 EXPORTED = ("rkv_n_ref", "rkv_query_sizes", "rkv_build_ref_pool", "rkv_compress",
             "rkv_gather_dequant", "rkv_restore_kv", "rkv_attention_workspace", "rkv_sparse_attention",
             "rkv_append_token", "rkv_compress_noalloc", "rkv_profile_enable", "rkv_profile_collect",
-            "rkv_status_string")
+            "rkv_debug_wait_fault", "rkv_status_string")
 _DTYPES = {"f32": RKV_F32, "bf16": RKV_BF16, "fp8": RKV_FP8_E4M3}
 
 
@@ -89,6 +89,8 @@ def lib():
         L.rkv_profile_collect.argtypes = [ctypes.c_char_p, I32, ctypes.POINTER(ctypes.c_float),
                                           ctypes.POINTER(I32), I32]
         L.rkv_profile_collect.restype = I32
+        L.rkv_debug_wait_fault.argtypes = [ctypes.c_int64, I32]
+        L.rkv_debug_wait_fault.restype = I32
         L.rkv_status_string.argtypes = [I32]
         L.rkv_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -211,6 +213,12 @@ def rkv_sparse_attention(p: rkv_params, H: int, q, k_hat, v_hat, sel, n_sel: int
                                     int(workspace_bytes), _stream(stream))
     if st:
         raise RkvError(st, "rkv_sparse_attention")
+
+
+def rkv_debug_wait_fault(wait_cycles: int, skip_use: int) -> None:
+    st = lib().rkv_debug_wait_fault(int(wait_cycles), int(skip_use))
+    if st:
+        raise RkvError(st, "rkv_debug_wait_fault")
 
 
 def rkv_profile_enable(on: bool) -> None:

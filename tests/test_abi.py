@@ -124,3 +124,9 @@ def test_restore_validates_on_the_host(lib):
     assert call(rkv.make_params(1, 1, 256, 2, 64, 256, 64, kv_dtype="f32")) == rkv.RKV_ERR_UNSUPPORTED
     assert call(rkv.make_params(1, 1, 256, 8, 128, 1024, 384)) == rkv.RKV_ERR_UNSUPPORTED   # d_c
     assert call(rkv.make_params(1, 1, 256, 2, 48, 1024, 512)) == rkv.RKV_ERR_UNSUPPORTED    # D
+
+
+def test_timeout_hook_validates_host_side(lib):
+    # the timeout-path test hook checks its arguments on the host (no GPU needed)
+    for cycles, skip in ((0, 0), (9999, 0), (3 * 10 ** 9, 0), (200000, -1)):
+        assert lib.rkv_debug_wait_fault(cycles, skip) == rkv.RKV_ERR_INVALID_ARG
