@@ -23,10 +23,12 @@ namespace rkv {
 // is accepted from the expansion only if its k-th/(k+1)-th gap exceeds twice
 // kTau * (max ||r||^2 + 2 ||x|| max ||r||); otherwise it is re-ranked with exact
 // differences.
-constexpr int kList = 8;                  // sorted list kept per row and column half
+constexpr int kList = 8;                  // sorted list kept per row and column half (>= k + 1)
 constexpr int kCand = 2 * kList;          // candidate entries per row and work item
 constexpr float kTau = 1.0f / 32768.0f;   // 2^-15
 constexpr int kMaxK = 4;                  // ref_idx rows are int4
+static_assert(kList >= kMaxK + 1 && kList % 2 == 0,
+              "a list must hold the (k+1)-th entry; entries go out as float4 pairs");
 
 // tcgen05 GEMM tiling: 128 token rows x 256 columns, K chunks of 64 bf16.
 constexpr int kBM = 128;

@@ -153,7 +153,7 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
             for (int j = 0; j <= kMaxK; ++j) { te[j] = INFINITY; ts[j] = kNoSlot; }
             float e_last = INFINITY;   // smallest last entry of a full list
             for (int ch = 0; ch < nch; ++ch) {
-                // the work item's two sorted lists, all 8 float4 loads in flight at once
+                // the work item's two sorted lists, all their float4 loads in flight at once
                 float4 e4[kCand / 2];
 #pragma unroll
                 for (int j = 0; j < kCand / 2; ++j) e4[j] = cp[ch * (kCand / 2) + j];

@@ -146,6 +146,23 @@ __device__ __forceinline__ int dist_cols(const UmmaArgs &a, int t, int n)
     return own >= kBN ? kBN : ((own + 31) & ~31);
 }
 
+// v[j] for a lane-dependent j in [0, 32), by a tree of selects: indexing the register
+// array with a runtime j would put it in local memory
+__device__ __forceinline__ float pick32(const float (&v)[32], int j)
+{
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (j & 16) ? v[i + 16] : v[i];
+    float b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = (j & 8) ? a[i + 8] : a[i];
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[i + 4] : b[i];
+    const float d0 = (j & 2) ? c[2] : c[0], d1 = (j & 2) ? c[3] : c[1];
+    return (j & 1) ? d1 : d0;
+}
+
 // Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
 __device__ __forceinline__ float silu_fast(float u)
 {
@@ -209,63 +226,70 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             um::prefetch_tmap(&tmA0);
             um::prefetch_tmap(&tmA1);
             um::prefetch_tmap(&tmB);
+            // The stage loop is kept short (no divisions, no memory reads): this one
+            // thread shares its scheduler with epilogue warps, and every cycle it loses
+            // delays a refill the MMA waits for.
             int stage = 0;
             uint32_t ph = 0;
-            uint32_t last_ph[S];
-            bool used[S];
-            for (int s = 0; s < S; ++s) { used[s] = false; last_ph[s] = 0; }
+            uint32_t used_mask = 0, ph_mask = 0;   // per stage: used, parity of its last use
             bool ok = true;
             int use = 0;
+            const int kx_end = a.k_chunks * kBK;
             for (int rnd = 0; rnd * npairs < n_items && ok; ++rnd) {
                 const int i = item_at(rnd, pid, npairs);
                 if (i >= n_items) continue;
                 Item it;
                 if (!item_get<MODE>(a, i, it)) continue;
+                const int lz = it.lb / a.B;                          // layer of the weights
+                const int own_rows = it.t * 2 * kBM + (int)rank * kBM;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
-                    for (int kc = 0; kc < k_iters; ++kc) {
-                        const bool w = um::mbar_wait(&empty[stage], ph ^ 1u, a.wait_cycles);
-                        if (*abort_flag || !w) {
-                            ok = false;
-                            break;
-                        }
-                        // test hook of the timeout path: the peer leaves one stage
-                        // short, so the leader's full barrier never completes
-                        if (!leader && use++ == a.skip_use) {
-                            used[stage] = true;
-                            last_ph[stage] = ph;
-                            if (++stage == S) { stage = 0; ph ^= 1u; }
-                            continue;
-                        }
-                        uint8_t *sa = tiles + stage * kStageBytes;
-                        uint8_t *sb = sa + kABytes;
-                        const uint32_t fb = um::smem_u32(&full[stage]);
-                        // the leader's full barrier counts both CTAs' bytes
-                        if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-                        const uint32_t bar = leader ? fb : um::mapa(fb, 0);
-                        const int src = kc / a.k_chunks;
-                        const int kx = (kc - src * a.k_chunks) * kBK;
-                        if (C::kT) {
-                            // A: 64 rows of W_c1 and the same 64 rows of W_c2; B: 128 tokens
-                            const int f0 = n * kBM + (int)rank * (kBM / 2);
-                            const int lz = it.lb / a.B;
-                            if (a.fused_gate) {
-                                um::tma_load_3d_pair(sa, &tmA0, bar, kx, lz * a.d_ff + f0, 0);
-                            } else {
-                                um::tma_load_3d_pair(sa, &tmA0, bar, kx, f0, lz);
-                                um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, f0, lz);
+                    if (*abort_flag) { ok = false; break; }
+                    // coordinates that stay fixed along K: A (y, z), B (y, z)
+                    int ay, az, by, bz;
+                    if (C::kT) {
+                        // A: 64 rows of W_c1 and the same 64 rows of W_c2; B: 128 tokens
+                        const int f0 = n * kBM + (int)rank * (kBM / 2);
+                        ay = a.fused_gate ? lz * a.d_ff + f0 : f0;
+                        az = a.fused_gate ? 0 : lz;
+                        by = own_rows;
+                        bz = it.lb;
+                    } else {
+                        // A: 128 token rows (M_S2: dh_hi, then dh_lo); B: half of N tile n
+                        ay = own_rows;
+                        az = it.lb;
+                        const int half = MODE == M_DIST ? dist_cols(a, it.t, n) / 2 : kHalfN;
+                        by = n * kBN + (int)rank * half;
+                        bz = MODE == M_S2 ? lz : it.lb;
+                    }
+                    for (int src = 0; src < a.a_sources && ok; ++src) {
+                        const CUtensorMap *mA = src ? &tmA1 : &tmA0;
+                        for (int kx = 0; kx < kx_end; kx += kBK) {
+                            if (!um::mbar_wait(&empty[stage], ph ^ 1u, a.wait_cycles)) {
+                                ok = false;
+                                break;
                             }
-                            um::tma_load_3d_pair(sb, &tmB, bar, kx, it.t * 2 * kBM + (int)rank * kBM, it.lb);
-                        } else {
-                            // A: 128 token rows (M_S2: dh_hi, then dh_lo); B: half of N tile n
-                            um::tma_load_3d_pair(sa, src ? &tmA1 : &tmA0, bar, kx,
-                                                 it.t * 2 * kBM + (int)rank * kBM, it.lb);
-                            const int half = MODE == M_DIST ? dist_cols(a, it.t, n) / 2 : kHalfN;
-                            um::tma_load_3d_pair(sb, &tmB, bar, kx, n * kBN + (int)rank * half,
-                                                 MODE == M_S2 ? it.lb / a.B : it.lb);
+                            used_mask |= 1u << stage;
+                            ph_mask = (ph_mask & ~(1u << stage)) | (ph << stage);
+                            // test hook of the timeout path: the peer leaves one stage
+                            // short, so the leader's full barrier never completes
+                            if (!leader && use++ == a.skip_use) {
+                                if (++stage == S) { stage = 0; ph ^= 1u; }
+                                continue;
+                            }
+                            uint8_t *sa = tiles + stage * kStageBytes;
+                            const uint32_t fb = um::smem_u32(&full[stage]);
+                            // the leader's full barrier counts both CTAs' bytes
+                            if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                            const uint32_t bar = leader ? fb : um::mapa(fb, 0);
+                            if (C::kT && !a.fused_gate) {
+                                um::tma_load_3d_pair(sa, &tmA0, bar, kx, ay, az);
+                                um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, ay, az);
+                            } else {
+                                um::tma_load_3d_pair(sa, mA, bar, kx, ay, az);
+                            }
+                            um::tma_load_3d_pair(sa + kABytes, &tmB, bar, kx, by, bz);
+                            if (++stage == S) { stage = 0; ph ^= 1u; }
                         }
-                        used[stage] = true;
-                        last_ph[stage] = ph;
-                        if (++stage == S) { stage = 0; ph ^= 1u; }
                     }
                 }
             }
@@ -275,7 +299,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             }
             // a stage's copies have landed once the pair's MMA has freed it
             for (int s = 0; s < S; ++s)
-                if (used[s]) um::mbar_wait(&empty[s], last_ph[s], a.wait_cycles);
+                if ((used_mask >> s) & 1u) um::mbar_wait(&empty[s], (ph_mask >> s) & 1u, a.wait_cycles);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -290,8 +314,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (!item_get<MODE>(a, i, it)) continue;
                 for (int n = it.n0; n < it.n1 && ok; ++n) {
                     const uint32_t buf = cnt & 1u, tph = (cnt >> 1) & 1u;
-                    const bool w = um::mbar_wait(&tempty[buf], tph ^ 1u, a.wait_cycles);
-                    if (*abort_flag || !w) {
+                    if (*abort_flag || !um::mbar_wait(&tempty[buf], tph ^ 1u, a.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -300,8 +323,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // distance tiles: only the references the tile's rows can see
                     const uint32_t id = MODE == M_DIST ? um::idesc_bf16_f32(2 * kBM, dist_cols(a, it.t, n)) : kIdesc;
                     for (int kc = 0; kc < k_iters; ++kc) {
-                        const bool wf = um::mbar_wait(&full[stage], ph, a.wait_cycles);
-                        if (*abort_flag || !wf) {
+                        if (!um::mbar_wait(&full[stage], ph, a.wait_cycles)) {
                             ok = false;
                             break;
                         }
@@ -472,40 +494,54 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
                 } else if (MODE == M_DIST) {
+                    // ||r||^2 of this half's 128 columns, loaded before the accumulator
+                    // reads (lane l holds column 32 cc + l of chunk cc)
                     const float *rn = a.ref_sqnorm + (size_t)it.lb * a.n_ref;
-#pragma unroll 1
-                    for (int c0 = h * kHalfN; c0 < (h + 1) * kHalfN; c0 += 32) {
+                    float rnv[kHalfN / 32];
+#pragma unroll
+                    for (int cc = 0; cc < kHalfN / 32; ++cc) {
+                        const int sl = n * kBN + h * kHalfN + cc * 32 + lane;
+                        rnv[cc] = sl < tile_pool ? __ldg(rn + sl) : 0.0f;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < kHalfN / 32; ++cc) {
+                        const int c0 = h * kHalfN + cc * 32;
                         const int s0 = n * kBN + c0;
                         if (s0 >= tile_pool) break;          // uniform over the warp
                         float v[32];
                         um::tmem_ld32(tb + c0, v);
-                        const float rn_l = (s0 + lane < a.n_ref) ? rn[s0 + lane] : 0.0f;
-                        // the columns whose expansion is below this row's current 8th
-                        // entry (a superset of those that will enter: the bound only falls)
+                        // the columns whose expansion is below this row's current last
+                        // entry (a superset of those that will enter: the bound only falls),
+                        // collected in four independent partial masks
                         const float thr = be[kList - 1];
-                        uint32_t hit = 0u;
+                        const int lim = pool - s0;           // columns j < lim are in the pool
+                        uint32_t hm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float rj = __shfl_sync(0xffffffffu, rn_l, j);
+                            const float rj = __shfl_sync(0xffffffffu, rnv[cc], j);
                             v[j] = fmaf(-2.0f, v[j], rj);
-                            hit |= (uint32_t)(s0 + j < pool && v[j] < thr) << j;
+                            hm[j & 3] |= (uint32_t)(j < lim && v[j] < thr) << j;
                         }
+                        uint32_t hit = (hm[0] | hm[1]) | (hm[2] | hm[3]);
                         // each lane inserts only its own hits, in increasing column order
-                        // (strict < keeps the lower slot ahead of an equal later one), so
-                        // the warp runs the insertion max-popcount times, not once per
-                        // column some lane needs
-                        while (hit) {
+                        // (strict < keeps the lower slot ahead of an equal later one).  The
+                        // warp runs max-popcount rounds, all lanes together and without
+                        // branches: a lane out of hits inserts +inf, which never enters, and
+                        // a hit that no longer beats the last entry passes through
+                        // unchanged.
+                        const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)__popc(hit));
+                        for (int rd = 0; rd < rounds; ++rd) {
                             const int j = __ffs(hit) - 1;
+                            float ce = hit ? pick32(v, j) : INFINITY;
                             hit &= hit - 1u;
-                            float ce = v[j];
-                            if (!(ce < be[kList - 1])) continue;
                             int cs = s0 + j;
 #pragma unroll
                             for (int qq = 0; qq < kList; ++qq) {
                                 const bool lt = ce < be[qq];
                                 const float te = lt ? be[qq] : ce;
                                 const int ts = lt ? bs[qq] : cs;
-                                if (lt) { be[qq] = ce; bs[qq] = cs; }
+                                be[qq] = lt ? ce : be[qq];
+                                bs[qq] = lt ? cs : bs[qq];
                                 ce = te;
                                 cs = ts;
                             }
