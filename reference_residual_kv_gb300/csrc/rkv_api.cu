@@ -62,9 +62,10 @@ Workspace workspace_layout(const Geometry &g)
     const size_t LB = (size_t)g.LB, T = (size_t)g.T, R = (size_t)g.n_ref;
     const bool tc = g.kv_dtype == RKV_BF16;
     w.ref_mma = take(g.ref_dtype == RKV_FP8_E4M3 ? LB * R * g.W * 2 : 0);
-    // one extra all-zero row after the last reference's row (padding for unused slots)
-    w.P1 = take((LB * R + 1) * g.d_ff * 4);
-    w.P2 = take((LB * R + 1) * g.d_ff * 4);
+    // one extra all-zero row after the last reference's row (padding for unused slots);
+    // the tensor-core path keeps both projections interleaved in P1 ({P1[f], P2[f]})
+    w.P1 = take((LB * R + 1) * g.d_ff * (tc ? 8 : 4));
+    w.P2 = take(tc ? 0 : (LB * R + 1) * g.d_ff * 4);
     w.rn_max = take(LB * 4);
     w.cand = take(tc ? LB * T * g.max_chunks * kCand * 8 : 0);
     w.copy_flag = take(LB * T);

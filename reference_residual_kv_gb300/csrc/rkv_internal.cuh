@@ -54,7 +54,7 @@ Geometry make_geometry(const rkv_params *p);
 // Workspace carve-up (offsets in bytes from the workspace base, 256-aligned).
 struct Workspace {
     size_t ref_mma;      // bf16 [LB][n_ref][W]   decoded FP8 references (FP8 only)
-    size_t P1, P2;       // f32  [LB][n_ref][d_ff]
+    size_t P1, P2;       // f32  [LB][n_ref][d_ff] (tensor-core path: P1 holds float2 {P1, P2})
     size_t rn_max;       // f32  [LB]
     size_t cand;         // f32x2 [LB][T][max_chunks][kCand]  (tensor-core path)
     size_t copy_flag;    // u8   [LB][T]  1: every chosen reference equals the token

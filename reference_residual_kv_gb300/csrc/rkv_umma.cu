@@ -16,7 +16,8 @@
 //               MMA works; a stage is free once the MMA and these warps are done
 //               with it (the top-k finalisation's distance bound needs the norms)
 // The epilogue is what differs between the four uses:
-//   M_P    P1 | P2 = R W_c1^T | R W_c2^T for each stored reference (fp32 out)
+//   M_P    P1 | P2 = R W_c1^T | R W_c2^T for each stored reference (fp32 out,
+//          interleaved per column: {P1[f], P2[f]})
 //   M_DIST ||r||^2 - 2 x.r for the causal pool of each token, best kList per row
 //          and column half
 //          [RKV §2.2 = Sec. IV-A; ||x||^2 is common to a row and left out]
@@ -53,7 +54,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kNormWarps = 4;                    // M_DIST: token-norm warps per CTA
 template <int MODE> constexpr int threads_of() { return kThreads + (MODE == M_DIST ? 32 * kNormWarps : 0); }
 constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epilogue warp
-constexpr int kS1Round = 8;                      // S1: tokens whose gathers are in flight at once
+constexpr int kS1Round = 4;                      // S1: tokens per round of gathers (one round ahead)
 constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
 constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(2 * kBM, kBN);
@@ -76,7 +77,7 @@ struct UmmaArgs {
     int k_chunks, a_sources;
     int fused_gate;       // M_P/M_S1: tmA0 maps W_c1 and W_c2 together (one box per stage)
     int W, d_ff, d_c, n_ref, bits;
-    float *P1, *P2;
+    float *P12;           // [LB * n_ref + 1][d_ff] of {x.W_c1[f], x.W_c2[f]} per reference
     const float *ref_sqnorm;
     const int32_t *pool_size, *ref_slot;
     float2 *cand;
@@ -161,6 +162,20 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int j)
     for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[i + 4] : b[i];
     const float d0 = (j & 2) ? c[2] : c[0], d1 = (j & 2) ? c[3] : c[1];
     return (j & 1) ? d1 : d0;
+}
+
+// 2^x and 1/x by the approximate hardware instructions (relative error ~2^-22)
+__device__ __forceinline__ float exp2f_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_fast(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
@@ -463,7 +478,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         live = 1.0f;
                     }
                     info[2 * (cc * 32 + lane)] = o;
-                    info[2 * (cc * 32 + lane) + 1] = make_int4(__float_as_int(inv_k), __float_as_int(live), 0, 0);
+                    // 1/k for a live token (0 when its pool is empty), -1 for a reference
+                    // token or an exact copy (dh = 0)
+                    info[2 * (cc * 32 + lane) + 1] = make_int4(__float_as_int(live > 0.0f ? inv_k : -1.0f), 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -480,7 +497,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (MODE == M_P) {
                     // lane = d_ff column f of W_c1 (q < 2) or W_c2, TMEM column = reference
                     const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
-                    float *P = (q < 2 ? a.P1 : a.P2) + (size_t)it.lb * a.n_ref * a.d_ff + f;
+                    float *P = a.P12 + ((size_t)it.lb * a.n_ref * a.d_ff + f) * 2 + (q < 2 ? 0 : 1);
 #pragma unroll 1
                     for (int cc = 0; cc < 4; ++cc) {
                         const int c0 = h * kHalfN + cc * 32;
@@ -490,7 +507,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (f < a.d_ff) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                if (r0 + j < a.rows) P[(size_t)(r0 + j) * a.d_ff] = v[j];
+                                if (r0 + j < a.rows) P[(size_t)(r0 + j) * a.d_ff * 2] = v[j];
                         }
                     }
                 } else if (MODE == M_DIST) {
@@ -554,13 +571,63 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const bool gate = q < 2;
                     const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
                     const bool fok = f < a.d_ff;
-                    const float *P1f = a.P1 + (fok ? f : 0);
-                    const float *P2f = a.P2 + (fok ? f : 0);
+                    const float2 *P12f = (const float2 *)a.P12 + (fok ? f : 0);
                     const int own0 = h * kHalfN + (gate ? 0 : 64);
                     const int give0 = h * kHalfN + (gate ? 64 : 0);
                     const int4 *info = info_buf + (warp - 2) * 128;
                     const int gb = 2 + 4 * h;                     // first warp of this half
                     const int me = warp - 2, partner = gb + ((warp - gb) ^ 2) - 2;
+                    // the chosen references' projection rows of 4 tokens, one round ahead
+                    // of the arithmetic (two register buffers)
+                    float2 pa[kS1Round][4], pb[kS1Round][4];
+                    float sa[kS1Round], sb[kS1Round];      // 1/k for a live token, else -1
+                    auto gather = [&](int c, float2 (&pr)[kS1Round][4], float (&sc)[kS1Round]) {
+#pragma unroll
+                        for (int u = 0; u < kS1Round; ++u) {
+                            const int4 o = info[2 * (c + u)];
+                            sc[u] = __int_as_float(info[2 * (c + u) + 1].x);
+                            pr[u][0] = __ldg(P12f + o.x);
+                            pr[u][1] = __ldg(P12f + o.y);
+                            pr[u][2] = __ldg(P12f + o.z);
+                            pr[u][3] = __ldg(P12f + o.w);
+                        }
+                    };
+                    // dh = Swish(g1) g2 - Swish(m1) m2 for 4 tokens, with Swish(u) =
+                    // u / (1 + e^-u) over one reciprocal of both denominators:
+                    //   dh = (g1 g2 (1 + e_m) - m1 m2 (1 + e_g)) / ((1 + e_g)(1 + e_m));
+                    // e^-u is clamped at 2^63 (u < -43.6: Swish is below 1e-17 there) so
+                    // the denominator stays finite.  A reference token or an exact copy
+                    // has scale -1, so dh = 0.
+                    auto finish = [&](int c, const float (&v)[kXTok], int v0, const float *xr,
+                                      const float2 (&pr)[kS1Round][4], const float (&sc)[kS1Round]) {
+                        const int t0 = it.t * 2 * kBM + own0 + c;
+                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+#pragma unroll
+                        for (int u = 0; u < kS1Round; ++u) {
+                            const float pv = xr[(v0 + u) * 32 + lane];
+                            const float g1 = gate ? v[v0 + u] : pv, g2 = gate ? pv : v[v0 + u];
+                            const float2 s01 = __fadd2_rn(pr[u][0], pr[u][1]);
+                            const float2 s23 = __fadd2_rn(pr[u][2], pr[u][3]);
+                            const float ik = fmaxf(sc[u], 0.0f);
+                            const float2 m = __fmul2_rn(__fadd2_rn(s01, s23), make_float2(ik, ik));
+                            const float2 t = __fmul2_rn(make_float2(g1, m.x),
+                                                        make_float2(-1.4426950408889634f, -1.4426950408889634f));
+                            const float eg = exp2f_fast(fminf(t.x, 63.0f));
+                            const float em = exp2f_fast(fminf(t.y, 63.0f));
+                            const float2 d = __fadd2_rn(make_float2(eg, em), make_float2(1.0f, 1.0f));
+                            const float2 pq = __fmul2_rn(make_float2(g1, m.x), make_float2(g2, m.y));
+                            const float num = fmaf(pq.x, d.y, -(pq.y * d.x));
+                            const float live = sc[u] >= 0.0f ? 1.0f : 0.0f;
+                            const float dh = num * rcp_fast(d.x * d.y) * live;
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
+                            if (fok && t0 + u < a.rows) {
+                                hi[(size_t)u * a.d_ff] = hb;
+                                lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                            }
+                        }
+                    };
+                    gather(0, pa, sa);
 #pragma unroll 1
                     for (int c = 0; c < 64; c += kXTok) {
                         // double-buffered: a buffer is rewritten only after the next
@@ -568,49 +635,19 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         float *xw = xbuf + (size_t)(((xcnt & 1u) * kEpiWarps + me) * kXTok) * 32;
                         const float *xr = xbuf + (size_t)(((xcnt & 1u) * kEpiWarps + partner) * kXTok) * 32;
                         ++xcnt;
+                        {
+                            float g[kXTok];
+                            um::tmem_ld8(tb + give0 + c, g);
 #pragma unroll
-                        for (int p8 = 0; p8 < kXTok; p8 += 8) {
-                            float g[8];
-                            um::tmem_ld8(tb + give0 + c + p8, g);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) xw[(p8 + j) * 32 + lane] = g[j];
+                            for (int j = 0; j < kXTok; ++j) xw[j * 32 + lane] = g[j];
                         }
                         um::bar_sync(pair_id, 64);
-#pragma unroll 1
-                        for (int r8 = 0; r8 < kXTok; r8 += kS1Round) {
-                            const int cc = c + r8;
-                            float x1[kS1Round][4], x2[kS1Round][4], ik[kS1Round], lv[kS1Round];
-#pragma unroll
-                            for (int u = 0; u < kS1Round; ++u) {
-                                const int4 o = info[2 * (cc + u)];
-                                const int4 b = info[2 * (cc + u) + 1];
-                                ik[u] = __int_as_float(b.x);
-                                lv[u] = __int_as_float(b.y);
-                                x1[u][0] = __ldg(P1f + o.x); x2[u][0] = __ldg(P2f + o.x);
-                                x1[u][1] = __ldg(P1f + o.y); x2[u][1] = __ldg(P2f + o.y);
-                                x1[u][2] = __ldg(P1f + o.z); x2[u][2] = __ldg(P2f + o.z);
-                                x1[u][3] = __ldg(P1f + o.w); x2[u][3] = __ldg(P2f + o.w);
-                            }
-                            float v[kS1Round];
-                            um::tmem_ld8(tb + own0 + cc, v);
-                            const int t0 = it.t * 2 * kBM + own0 + cc;
-                            __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
-                            __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
-#pragma unroll
-                            for (int u = 0; u < kS1Round; ++u) {
-                                const float pv = xr[(r8 + u) * 32 + lane];
-                                const float g1 = gate ? v[u] : pv, g2 = gate ? pv : v[u];
-                                const float m1 = ((x1[u][0] + x1[u][1]) + (x1[u][2] + x1[u][3])) * ik[u];
-                                const float m2 = ((x2[u][0] + x2[u][1]) + (x2[u][2] + x2[u][3])) * ik[u];
-                                // reference token or exact copy: lv = 0, z = 0
-                                const float dh = (silu_fast(g1) * g2 - silu_fast(m1) * m2) * lv[u];
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
-                                if (fok && t0 + u < a.rows) {
-                                    hi[(size_t)u * a.d_ff] = hb;
-                                    lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
-                                }
-                            }
-                        }
+                        float v[kXTok];
+                        um::tmem_ld8(tb + own0 + c, v);
+                        gather(c + kS1Round, pb, sb);
+                        finish(c, v, 0, xr, pa, sa);
+                        if (c + kXTok < 64) gather(c + kXTok, pa, sa);
+                        finish(c + kS1Round, v, kS1Round, xr, pb, sb);
                     }
                 } else {  // M_S2
 #pragma unroll 1
@@ -804,16 +841,16 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
                                  float *z_out, int32_t *status, cudaStream_t s)
 {
     cudaError_t e;
-    float *P1 = (float *)(ws + wl.P1), *P2 = (float *)(ws + wl.P2);
+    float *P12 = (float *)(ws + wl.P1);                        // interleaved {P1, P2}
     float *rn_max = (float *)(ws + wl.rn_max);
     float2 *cand = (float2 *)(ws + wl.cand);
     __nv_bfloat16 *dh_hi = (__nv_bfloat16 *)(ws + wl.dh_hi);
     __nv_bfloat16 *dh_lo = (__nv_bfloat16 *)(ws + wl.dh_lo);
     const bool fp8 = g.ref_dtype == RKV_FP8_E4M3;
     void *ref_mma = fp8 ? (void *)(ws + wl.ref_mma) : pool->ref_vec;
-    const size_t zrow = (size_t)g.LB * g.n_ref * g.d_ff;     // the all-zero projection row
+    const size_t zrow = (size_t)g.LB * g.n_ref * g.d_ff * 2; // the all-zero projection row
     float *xnorm = (float *)(ws + wl.xnorm);
-    if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, P1 + zrow, P2 + zrow, s)) != cudaSuccess)
+    if ((e = launch_prep_refs(g, pool, ref_mma, rn_max, P12 + zrow, P12 + zrow + g.d_ff, s)) != cudaSuccess)
         return e;
 
     UmmaArgs a{};
@@ -821,7 +858,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     a.skip_use = -1;
     a.LB = g.LB; a.B = g.B; a.T = g.T; a.W = g.W; a.d_ff = g.d_ff; a.d_c = g.d_c;
     a.n_ref = g.n_ref; a.bits = g.bits;
-    a.P1 = P1; a.P2 = P2; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
+    a.P12 = P12; a.ref_sqnorm = pool->ref_sqnorm; a.pool_size = pool->pool_size;
     a.ref_slot = pool->ref_slot; a.cand = cand; a.ref_idx = (const int4 *)cache->ref_idx;
     uint8_t *copy_flag = ws + wl.copy_flag;
     a.copy_flag = copy_flag;
