@@ -26,11 +26,14 @@
 //          by linearity [RKV §2.2, §2.3 = Sec. IV-A]; stored as bf16 hi + lo
 //   M_S2   z = dh_hi W_c3 + dh_lo W_c3 = f_c(kv) - f_c(mean), then per-token
 //          group min/max quantisation and packing [RKV §2.4]
-// M_P and M_S1 run transposed (weights on the MMA's M side, tokens on N): each CTA's
-// 128 A rows are 64 rows of W_c1 and the same 64 rows of W_c2, so TMEM lane l < 64
-// holds x.W_c1[f] and lane 64 + l holds x.W_c2[f] of one d_ff column f, and a warp's
-// 32 lanes are 32 consecutive f: the epilogue's per-token gathers of reference
-// projections and its stores are 128-byte lines.
+// M_P and M_S1 run transposed (weights on the MMA's M side, tokens on N), each CTA's 128
+// A rows covering 64 d_ff columns of W_c1 and W_c2.  In M_S1 they are 64 rows of W_c1
+// and the same 64 rows of W_c2, so TMEM lane l < 64 holds x.W_c1[f] and lane 64 + l
+// holds x.W_c2[f] of one column f, and a warp's 32 lanes are 32 consecutive f: the
+// epilogue's per-token gathers of reference projections and its stores are contiguous
+// runs.  In M_P each 32-row lane quarter is 16 rows of W_c1 and then the same 16 rows of
+// W_c2, so lanes l and l + 16 write the two halves of one {P1[f], P2[f]} pair and a
+// warp's stores are contiguous 128-byte runs.
 // Every mbarrier wait is bounded; on expiry the kernel reports
 // RKV_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and returns.
 #include "rkv_exact.cuh"
@@ -57,6 +60,7 @@ constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epi
 constexpr int kS1Round = 4;                      // S1: tokens per round of gathers (one round ahead)
 constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
 constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
+constexpr int kGateRows = 16;                    // M_P: W_c1 rows, then the same W_c2 rows, per lane quarter
 constexpr uint32_t kIdesc = um::idesc_bf16_f32(2 * kBM, kBN);
 constexpr uint16_t kPairMask = 3;
 
@@ -262,9 +266,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // coordinates that stay fixed along K: A (y, z), B (y, z)
                     int ay, az, by, bz;
                     if (C::kT) {
-                        // A: 64 rows of W_c1 and the same 64 rows of W_c2; B: 128 tokens
+                        // A: 64 d_ff columns of W_c1 and W_c2 (M_P: in 16-row groups);
+                        // B: 128 tokens or references
                         const int f0 = n * kBM + (int)rank * (kBM / 2);
-                        ay = a.fused_gate ? lz * a.d_ff + f0 : f0;
+                        ay = a.fused_gate ? (MODE == M_P ? (lz * a.d_ff + f0) / kGateRows : lz * a.d_ff + f0) : f0;
                         az = a.fused_gate ? 0 : lz;
                         by = own_rows;
                         bz = it.lb;
@@ -296,7 +301,19 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             // the leader's full barrier counts both CTAs' bytes
                             if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
                             const uint32_t bar = leader ? fb : um::mapa(fb, 0);
-                            if (C::kT && !a.fused_gate) {
+                            if (MODE == M_P && a.fused_gate) {
+                                // [4 groups][W_c1, W_c2][16 rows] in one box
+                                um::tma_load_4d_pair(sa, &tmA0, bar, kx, 0, 0, ay);
+                            } else if (MODE == M_P) {
+                                // the same order from two separate matrices, 16 rows a box
+#pragma unroll
+                                for (int g = 0; g < kBM / (2 * kGateRows); ++g) {
+                                    uint8_t *dg = sa + g * 2 * kGateRows * 128;
+                                    um::tma_load_3d_pair(dg, &tmA0, bar, kx, ay + g * kGateRows, az);
+                                    um::tma_load_3d_pair(dg + kGateRows * 128, &tmA1, bar, kx,
+                                                         ay + g * kGateRows, az);
+                                }
+                            } else if (C::kT && !a.fused_gate) {
                                 um::tma_load_3d_pair(sa, &tmA0, bar, kx, ay, az);
                                 um::tma_load_3d_pair(sa + kABytes / 2, &tmA1, bar, kx, ay, az);
                             } else {
@@ -495,9 +512,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const uint32_t tb = tl + buf * kBN;
 
                 if (MODE == M_P) {
-                    // lane = d_ff column f of W_c1 (q < 2) or W_c2, TMEM column = reference
-                    const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
-                    float *P = a.P12 + ((size_t)it.lb * a.n_ref * a.d_ff + f) * 2 + (q < 2 ? 0 : 1);
+                    // lane l: d_ff column f of W_c1 (l < 16) or W_c2 (l >= 16); TMEM column =
+                    // reference
+                    const int f = n * kBM + (int)rank * (kBM / 2) + q * kGateRows + (lane & 15);
+                    float *P = a.P12 + ((size_t)it.lb * a.n_ref * a.d_ff + f) * 2 + (lane >> 4);
 #pragma unroll 1
                     for (int cc = 0; cc < 4; ++cc) {
                         const int c0 = h * kHalfN + cc * 32;
@@ -788,6 +806,24 @@ static bool make_map_gates(CUtensorMap *m, const void *W1, long long gate_off, u
     return r == CUDA_SUCCESS;
 }
 
+// The same two matrices as a 4-D tensor [L*d_ff/16 groups][2 matrices][16 rows][W]:
+// box = 64 (inner) x 16 rows x both matrices x 4 groups, i.e. per 32-row quarter 16 rows
+// of W_c1 followed by the same 16 rows of W_c2 (the reference-projection layout).
+static bool make_map_gates16(CUtensorMap *m, const void *W1, long long gate_off, uint64_t inner,
+                             uint64_t rows, uint64_t layers)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {inner, (cuuint64_t)kGateRows, 2, rows * layers / kGateRows};
+    cuuint64_t strides[3] = {inner * 2, (cuuint64_t)gate_off, inner * 2 * kGateRows};
+    cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kGateRows, 2, (cuuint32_t)(kBM / (2 * kGateRows))};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(W1), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int MODE>
 static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                        const UmmaArgs &args, cudaStream_t s)
@@ -886,13 +922,25 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         if (!make_map_gates(&mG1, W1t, gate_off, g.W, g.d_ff, g.L)) return cudaErrorInvalidValue;
         a.fused_gate = 1;
     }
+    // the reference projections take the 16-row-group layout: one 4-D box per stage
+    // when the gates are fused and d_ff is a multiple of 16, else 16-row boxes
+    const bool fused16 = fused && g.d_ff % kGateRows == 0;
+    CUtensorMap mP1, mP2;
+    if (fused16) {
+        if (!make_map_gates16(&mP1, W1t, gate_off, g.W, g.d_ff, g.L)) return cudaErrorInvalidValue;
+        mP2 = mP1;
+    } else if (!make_map(&mP1, W1t, g.W, g.d_ff, g.L, kGateRows) ||
+               !make_map(&mP2, W2t, g.W, g.d_ff, g.L, kGateRows)) {
+        return cudaErrorInvalidValue;
+    }
     if (g.n_ref > 0) {
         if (!make_map(&mR, ref_mma, g.W, g.n_ref, g.LB, kHalfN)) return cudaErrorInvalidValue;
         // P1 | P2 for every reference
         UmmaArgs p = a;
         p.rows = g.n_ref; p.tiles_t = (g.n_ref + kTileM - 1) / kTileM; p.tiles_n = ff_slices;
         p.k_chunks = kw; p.a_sources = 1;
-        if ((e = run<M_P>(mG1, mW2, mR, p, s)) != cudaSuccess) return e;
+        p.fused_gate = fused16 ? 1 : 0;
+        if ((e = run<M_P>(mP1, mP2, mR, p, s)) != cudaSuccess) return e;
         // distance expansion and per-item candidates
         UmmaArgs d = a;
         d.rows = g.T; d.tiles_t = g.n_mtiles; d.tiles_n = g.max_chunks;
