@@ -316,8 +316,9 @@ def test_gather_standalone_padding_and_isolation():
     assert torch.equal(zp, zs) and torch.equal(mp, ms)
 
 
-def test_gather_out_of_range_index_is_reported_not_faulted():
-    cfg = C["tiny-fp32"]
+@pytest.mark.parametrize("name", ["tiny-fp32", "long-fp8-1x1500"])
+def test_gather_out_of_range_index_is_reported_not_faulted(name):
+    cfg = C[name] if name in C else SMALL[name]
     kv, w = gen_inputs(cfg)
     bufs, _ = run_gpu(cfg, kv, w)
     sel = torch.tensor([[0, 5, cfg.T, 7]], dtype=torch.int32, device="cuda")
