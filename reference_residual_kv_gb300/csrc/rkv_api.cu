@@ -71,6 +71,7 @@ Workspace workspace_layout(const Geometry &g)
     w.copy_flag = take(LB * T);
     w.xnorm = take(tc ? LB * T * 4 : 0);
     w.scan_list = take(tc ? (LB * T + 1) * 4 : 0);     // list, then its count
+    w.rr_list = take(tc ? LB * T * 8 + 8 : 0);         // list, then its count
     w.dh_hi = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh_lo = take(tc ? LB * T * g.d_ff * 2 : 0);
     w.dh32 = take(tc ? 0 : LB * T * g.d_ff * 4);

@@ -60,6 +60,7 @@ struct Workspace {
     size_t copy_flag;    // u8   [LB][T]  1: every chosen reference equals the token
     size_t xnorm;        // f32  [LB][T]  ||x||^2 of every token (tensor-core path)
     size_t scan_list;    // i32  [LB*T] tokens whose top-k needs a full exact scan, + count
+    size_t rr_list;      // i32x2 [LB*T] tokens to re-rank or copy-check exactly, + count
     size_t dh_hi, dh_lo; // bf16 [LB][T][d_ff]   (tensor-core path)
     size_t dh32;         // f32  [LB][T][d_ff]   (fp32 path)
     size_t z32;          // f32  [LB][T][d_c]    (fp32 path)
@@ -94,7 +95,8 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
                                  const float2 *cand, const float *xnorm, const float *rn_max,
                                  int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
-                                 int32_t *scan_count, int32_t *status, cudaStream_t s);
+                                 int32_t *scan_count, int2 *rr_list, int32_t *rr_count,
+                                 int32_t *status, cudaStream_t s);
 
 int device_sm_count();
 

@@ -210,7 +210,8 @@ cudaError_t launch_simt_compress(const Geometry &g, const void *kv, const rkv_re
     }
     uint8_t *copy_flag = ws + wl.copy_flag;
     if ((e = launch_topk_finalize(g, kv, pool->ref_vec, 1, pool, nullptr, nullptr, rn_max,
-                                  cache->ref_idx, copy_flag, nullptr, nullptr, status, s)) != cudaSuccess)
+                                  cache->ref_idx, copy_flag, nullptr, nullptr, nullptr, nullptr,
+                                  status, s)) != cudaSuccess)
         return e;
     {
         dim3 grid((g.d_ff + 31) / 32, (g.T + 63) / 64, g.LB);

@@ -4,15 +4,19 @@
 //
 // The tensor-core pass ranks references by the expansion ||r||^2 - 2 x.r (the
 // ||x||^2 term is common to a row); every work item leaves two sorted lists of its
-// kList best per token.  Here one thread per token merges those lists and decides:
+// kList best per token.  Here one thread per token merges those lists and decides
+// (k_topk_select):
 //   * if the k-th/(k+1)-th expansion gap exceeds twice the expansion error bound
 //     E = kTau (rmax + 2 sqrt(||x||^2 rmax)), rmax = max ||r||^2 of the sequence,
 //     the expansion's top-k is the exact top-k;
 //   * else, if every possible member of the exact top-k is among the entries (no
 //     full list ends inside the band e <= e_k + 2E), the entries inside the band are
-//     re-ranked by exact distances (the warp serves such tokens one after another);
+//     re-ranked by exact distances: the token goes on a queue that k_topk_rerank serves
+//     with one warp per token (two distances in flight), so that warps holding many such
+//     tokens do not serialise the pass;
 //   * else every reference of the pool is scanned with exact distances.
-// It also flags tokens that are bit-identical to every chosen reference: their mean
+// It also flags tokens that are bit-identical to every chosen reference (checked with
+// exact distances on the same queue, only where the expansion allows it): their mean
 // equals the token exactly, so z = 0 exactly [RKV §2.3], which the encoder then
 // writes directly (the tensor cores need not round the token's and the
 // references' projections identically, since they sit in different tile rows).
@@ -123,7 +127,8 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
               const float2 *__restrict__ cand, const float *__restrict__ xnorm,
               const float *__restrict__ rn_max, int LB, int T_, int W, int n_ref, int k,
               int max_chunks, int4 *__restrict__ ref_idx, uint8_t *__restrict__ copy_flag,
-              int32_t *__restrict__ scan_list, int32_t *__restrict__ scan_count)
+              int32_t *__restrict__ scan_list, int32_t *__restrict__ scan_count,
+              int2 *__restrict__ rr_list, int32_t *__restrict__ rr_count)
 {
     enum { kNone = 0, kDone, kRerank, kCopyCheck, kFull };
     const int lane = threadIdx.x & 31;
@@ -140,9 +145,27 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
             ch[0] = own;
             state = kDone;
         } else if (pool <= k) {
+            // every reference of the pool is chosen; the token can equal all of them only
+            // if the expansion puts each within the error bound of distance 0 (the lists
+            // hold every pool member, pool <= k < kList)
 #pragma unroll
             for (int j = 0; j < kMaxK; ++j) ch[j] = j < pool ? j : kNoSlot;
-            state = pool > 0 ? kCopyCheck : kDone;
+            state = kDone;
+            if (pool > 0) {
+                const float4 *cp = (const float4 *)(cand + (size_t)gt * max_chunks * kCand);
+                float e_max = -INFINITY;
+                int seen = 0;
+#pragma unroll
+                for (int j = 0; j < kCand / 2; ++j) {
+                    const float4 c = cp[j];
+                    if (__float_as_int(c.y) >= 0 && __float_as_int(c.y) < pool) { e_max = fmaxf(e_max, c.x); ++seen; }
+                    if (__float_as_int(c.w) >= 0 && __float_as_int(c.w) < pool) { e_max = fmaxf(e_max, c.z); ++seen; }
+                }
+                const float xn = xnorm[gt];
+                const float rm = rn_max[lb];
+                const float E = kTau * (rm + 2.0f * sqrtf(xn * rm));
+                if (seen != pool || xn + e_max <= 2.0f * E) state = kCopyCheck;
+            }
         } else {
             const int nch = (dist_ntiles(pool_size, T_, t / kTileM) + kDistChunk - 1) / kDistChunk;
             nlists = 2 * nch;
@@ -194,54 +217,86 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
         }
         if (state == kDone) store_choice(ref_idx, copy_flag, gt, ch, 0);
         if (state == kFull) scan_list[atomicAdd(scan_count, 1)] = (int32_t)gt;
+        if (state == kCopyCheck) {
+            // the choice is final; k_topk_rerank confirms or clears the copy flag
+            store_choice(ref_idx, copy_flag, gt, ch, 0);
+            rr_list[atomicAdd(rr_count, 1)] = make_int2((int)((uint32_t)gt | 0x80000000u), 0);
+        }
+        if (state == kRerank) rr_list[atomicAdd(rr_count, 1)] = make_int2((int)gt, __float_as_int(band));
     }
+}
 
-    unsigned need = __ballot_sync(0xffffffffu, state == kRerank || state == kCopyCheck);
-    while (need) {
-        const int src = __ffs(need) - 1;
-        need &= need - 1;
-        const int st = __shfl_sync(0xffffffffu, state, src);
-        const long long g = __shfl_sync(0xffffffffu, gt, src);
-        const int glb = __shfl_sync(0xffffffffu, lb, src);
+// The queued tokens of k_topk_select, one warp each: a copy check computes the exact
+// distances to the chosen references (the copy flag is set only if all are 0); a
+// re-rank computes the exact distances of the list entries inside the band, two at a
+// time, and keeps the k nearest (ties to the lower slot).
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_topk_rerank(const T *__restrict__ kv, const T *__restrict__ refs,
+              const int32_t *__restrict__ pool_size, const float2 *__restrict__ cand, int T_, int W,
+              int n_ref, int k, int max_chunks, const int2 *__restrict__ rr_list,
+              const int32_t *__restrict__ rr_count, int4 *__restrict__ ref_idx,
+              uint8_t *__restrict__ copy_flag)
+{
+    const int lane = threadIdx.x & 31;
+    const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+    const int n = *rr_count;
+    for (int e = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); e < n; e += nw) {
+        const int2 ent = rr_list[e];
+        const bool copy = ent.x < 0;
+        const long long g = (long long)((uint32_t)ent.x & 0x7fffffffu);
+        const int glb = (int)(g / T_), t = (int)(g % T_);
         const T *x = kv + (size_t)g * W;
         const T *rb = refs + (size_t)glb * n_ref * W;
         int cs[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) cs[j] = __shfl_sync(0xffffffffu, ch[j], src);
         int same = 1;
-        if (st == kCopyCheck) {
+        if (copy) {
+            const int4 c4 = ref_idx[g];
+            const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int j = 0; j < kMaxK; ++j)
-                if (cs[j] != kNoSlot) same &= warp_sqdist(x, rb + (size_t)cs[j] * W, W, lane) == 0.0f;
-        } else {
-            const float bd = __shfl_sync(0xffffffffu, band, src);
-            const int nent = __shfl_sync(0xffffffffu, nlists, src) * kList;
-            const float2 *cp = cand + (size_t)g * max_chunks * kCand;
-            float be[kMaxK];
-            int bs[kMaxK];
+                if (cc[j] >= 0) same &= warp_sqdist(x, rb + (size_t)cc[j] * W, W, lane) == 0.0f;
+            if (lane == 0) copy_flag[g] = (uint8_t)same;
+            continue;
+        }
+        const float bd = __int_as_float(ent.y);
+        const int nch = (dist_ntiles(pool_size, T_, t / kTileM) + kDistChunk - 1) / kDistChunk;
+        const int nent = 2 * nch * kList;
+        const float2 *cp = cand + (size_t)g * max_chunks * kCand;
+        float be[kMaxK];
+        int bs[kMaxK];
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = kNoSlot; }
-            for (int b = 0; b < nent; b += 32) {
-                float e = INFINITY;
-                int sl = -1;
-                if (b + lane < nent) {
-                    const float2 c = cp[b + lane];
-                    e = c.x;
-                    sl = __float_as_int(c.y);
-                }
-                unsigned in = __ballot_sync(0xffffffffu, sl >= 0 && e <= bd);
-                while (in) {
-                    const int q = __ffs(in) - 1;
+        for (int j = 0; j < kMaxK; ++j) { be[j] = INFINITY; bs[j] = kNoSlot; }
+        for (int b = 0; b < nent; b += 32) {
+            float ev = INFINITY;
+            int sl = -1;
+            if (b + lane < nent) {
+                const float2 c = cp[b + lane];
+                ev = c.x;
+                sl = __float_as_int(c.y);
+            }
+            unsigned in = __ballot_sync(0xffffffffu, sl >= 0 && ev <= bd);
+            while (in) {
+                const int q0 = __ffs(in) - 1;
+                in &= in - 1;
+                const int s0 = __shfl_sync(0xffffffffu, sl, q0);
+                if (in) {
+                    const int q1 = __ffs(in) - 1;
                     in &= in - 1;
-                    const int s = __shfl_sync(0xffffffffu, sl, q);
-                    list_insert<kMaxK>(be, bs, warp_sqdist(x, rb + (size_t)s * W, W, lane), s);
+                    const int s1 = __shfl_sync(0xffffffffu, sl, q1);
+                    float d0, d1;
+                    warp_sqdist2(x, rb + (size_t)s0 * W, rb + (size_t)s1 * W, W, lane, d0, d1);
+                    list_insert<kMaxK>(be, bs, d0, s0);
+                    list_insert<kMaxK>(be, bs, d1, s1);
+                } else {
+                    list_insert<kMaxK>(be, bs, warp_sqdist(x, rb + (size_t)s0 * W, W, lane), s0);
                 }
             }
+        }
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                cs[j] = j < k ? bs[j] : kNoSlot;
-                if (j < k) same &= be[j] == 0.0f;
-            }
+        for (int j = 0; j < kMaxK; ++j) {
+            cs[j] = j < k ? bs[j] : kNoSlot;
+            if (j < k) same &= be[j] == 0.0f;
         }
         if (lane == 0) store_choice(ref_idx, copy_flag, g, cs, same);
     }
@@ -323,13 +378,16 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
                                  int ref_exact_is_f32, const rkv_ref_pool *pool,
                                  const float2 *cand, const float *xnorm, const float *rn_max,
                                  int32_t *ref_idx, uint8_t *copy_flag, int32_t *scan_list,
-                                 int32_t *scan_count, int32_t *status, cudaStream_t s)
+                                 int32_t *scan_count, int2 *rr_list, int32_t *rr_count,
+                                 int32_t *status, cudaStream_t s)
 {
     (void)status;
     long long warps = (long long)g.LB * g.T;
     unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     cudaError_t e;
     if (scan_list && (e = cudaMemsetAsync(scan_count, 0, sizeof(int32_t), s)) != cudaSuccess)
+        return e;
+    if (rr_list && (e = cudaMemsetAsync(rr_count, 0, sizeof(int32_t), s)) != cudaSuccess)
         return e;
     {
         ProfScope prof("topk_finalize", s);
@@ -338,7 +396,7 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
             k_topk_select<__nv_bfloat16><<<tb, 256, 0, s>>>(
                 (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
                 pool->pool_size, cand, xnorm, rn_max, g.LB, g.T, g.W, g.n_ref, g.k,
-                g.max_chunks, (int4 *)ref_idx, copy_flag, scan_list, scan_count);
+                g.max_chunks, (int4 *)ref_idx, copy_flag, scan_list, scan_count, rr_list, rr_count);
         } else if (ref_exact_is_f32) {
             k_topk_scan_warp<float><<<blocks, 256, 0, s>>>(
                 (const float *)kv, (const float *)ref_exact, pool->ref_slot, pool->pool_size,
@@ -348,6 +406,13 @@ cudaError_t launch_topk_finalize(const Geometry &g, const void *kv, const void *
                 (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->ref_slot,
                 pool->pool_size, g.LB, g.T, g.W, g.n_ref, g.k, (int4 *)ref_idx, copy_flag);
         }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (cand && rr_list) {
+        ProfScope prof("topk_rerank", s);
+        k_topk_rerank<__nv_bfloat16><<<4 * device_sm_count(), 256, 0, s>>>(
+            (const __nv_bfloat16 *)kv, (const __nv_bfloat16 *)ref_exact, pool->pool_size, cand, g.T,
+            g.W, g.n_ref, g.k, g.max_chunks, rr_list, rr_count, (int4 *)ref_idx, copy_flag);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (scan_list) {

@@ -949,9 +949,10 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         if ((e = run<M_DIST>(mX, mX, mR, d, s)) != cudaSuccess) return e;
     }
     int32_t *scan_list = (int32_t *)(ws + wl.scan_list);
+    int2 *rr_list = (int2 *)(ws + wl.rr_list);
     if ((e = launch_topk_finalize(g, kv, ref_mma, 0, pool, cand, xnorm, rn_max, cache->ref_idx,
-                                  copy_flag, scan_list, scan_list + (size_t)g.LB * g.T, status,
-                                  s)) != cudaSuccess)
+                                  copy_flag, scan_list, scan_list + (size_t)g.LB * g.T, rr_list,
+                                  (int32_t *)(rr_list + (size_t)g.LB * g.T), status, s)) != cudaSuccess)
         return e;
     {
         UmmaArgs p = a;
