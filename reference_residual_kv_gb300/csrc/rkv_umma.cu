@@ -595,10 +595,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const int4 *info = info_buf + (warp - 2) * 128;
                     const int gb = 2 + 4 * h;                     // first warp of this half
                     const int me = warp - 2, partner = gb + ((warp - gb) ^ 2) - 2;
-                    // the chosen references' projection rows of 4 tokens, one round ahead
-                    // of the arithmetic (two register buffers)
-                    float2 pa[kS1Round][4], pb[kS1Round][4];
-                    float sa[kS1Round], sb[kS1Round];      // 1/k for a live token, else -1
+                    // the chosen references' projection pairs of 4 tokens per round, two
+                    // rounds ahead of the arithmetic (a ring of three register buffers; the
+                    // loop below is unrolled so that every buffer index is static)
+                    float2 pr3[3][kS1Round][4];
+                    float sc3[3][kS1Round];                // 1/k for a live token, else -1
                     auto gather = [&](int c, float2 (&pr)[kS1Round][4], float (&sc)[kS1Round]) {
 #pragma unroll
                         for (int u = 0; u < kS1Round; ++u) {
@@ -645,8 +646,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             }
                         }
                     };
-                    gather(0, pa, sa);
-#pragma unroll 1
+                    gather(0, pr3[0], sc3[0]);
+                    gather(kS1Round, pr3[1], sc3[1]);
+#pragma unroll
                     for (int c = 0; c < 64; c += kXTok) {
                         // double-buffered: a buffer is rewritten only after the next
                         // exchange barrier, which the partner reaches after reading it
@@ -662,10 +664,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         um::bar_sync(pair_id, 64);
                         float v[kXTok];
                         um::tmem_ld8(tb + own0 + c, v);
-                        gather(c + kS1Round, pb, sb);
-                        finish(c, v, 0, xr, pa, sa);
-                        if (c + kXTok < 64) gather(c + kXTok, pa, sa);
-                        finish(c + kS1Round, v, kS1Round, xr, pb, sb);
+                        const int r0 = c / kS1Round;       // rounds r0 and r0 + 1 of this exchange
+                        if (c + 2 * kS1Round < 64) gather(c + 2 * kS1Round, pr3[(r0 + 2) % 3], sc3[(r0 + 2) % 3]);
+                        finish(c, v, 0, xr, pr3[r0 % 3], sc3[r0 % 3]);
+                        if (c + 3 * kS1Round < 64) gather(c + 3 * kS1Round, pr3[(r0 + 3) % 3], sc3[(r0 + 3) % 3]);
+                        finish(c + kS1Round, v, kS1Round, xr, pr3[(r0 + 1) % 3], sc3[(r0 + 1) % 3]);
                     }
                 } else {  // M_S2
 #pragma unroll 1
