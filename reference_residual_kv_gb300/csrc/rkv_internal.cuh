@@ -35,7 +35,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kTileM = 2 * kBM;          // token rows of a CTA-pair tile (2-SM MMA, M = 256)
-constexpr int kDistChunk = 8;             // N-tiles (2048 references) per distance work item
+constexpr int kDistChunk = 16;            // N-tiles (4096 references) per distance work item
 
 // Bounded waits: ~1 s at 2 GHz.
 constexpr long long kWaitCycles = 2000000000LL;
