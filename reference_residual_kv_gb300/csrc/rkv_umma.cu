@@ -61,7 +61,6 @@ constexpr int kS1Round = 4;                      // S1: tokens per round of gath
 constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
 constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
 constexpr int kGateRows = 16;                    // M_P: W_c1 rows, then the same W_c2 rows, per lane quarter
-constexpr uint32_t kIdesc = um::idesc_bf16_f32(2 * kBM, kBN);
 constexpr uint16_t kPairMask = 3;
 
 template <int MODE> struct Cfg {
@@ -168,6 +167,14 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int j)
     return (j & 1) ? d1 : d0;
 }
 
+// S1: offset, from the warp's first token, of the token in its j-th own accumulator
+// column; with reference rows skipped (kG > 0) a column group of kG - 1 covers kG tokens
+template <int kG>
+__host__ __device__ constexpr int s1_token(int j)
+{
+    return kG > 0 ? (j / (kG - 1)) * kG + j % (kG - 1) + 1 : j;
+}
+
 // 2^x and 1/x by the approximate hardware instructions (relative error ~2^-22)
 __device__ __forceinline__ float exp2f_fast(float x)
 {
@@ -188,13 +195,22 @@ __device__ __forceinline__ float silu_fast(float u)
     return __fdividef(u, 1.0f + __expf(-u));
 }
 
-template <int MODE>
+// S1 with kG > 0: every position that is 0 mod kG is a reference (fixed stride dividing
+// kG, first reference at 0), where dh = 0.  Those token rows are not loaded: tmB is then
+// a [LB][T/kG][kG][W] view, each CTA's B half holds rows 1..kG-1 of its 128/kG groups
+// (kBRows rows), and the MMA's N is 2 kBRows.  TMEM column j of half h is token
+// h*128 + (j / (kG-1)) kG + j % (kG-1) + 1 of the tile.
+template <int MODE, int kG>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmB, const UmmaArgs a)
 {
     using C = Cfg<MODE>;
     constexpr int S = C::kStages;
+    constexpr bool kSkip = MODE == M_S1 && kG > 0;
+    constexpr int kBRows = kSkip ? kHalfN * (kG - 1) / kG : kHalfN;
+    static_assert(!kSkip || (kHalfN % (kSkip ? kG : 1) == 0 && (kBRows / 2) % kXTok == 0 && kBRows % 8 == 0),
+                  "skip layout: whole groups per CTA, whole exchanges per warp");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = smem_raw + ((1024u - (um::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = (uint64_t *)(tiles + S * kStageBytes);   // leader's: both CTAs' bytes
@@ -299,7 +315,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             uint8_t *sa = tiles + stage * kStageBytes;
                             const uint32_t fb = um::smem_u32(&full[stage]);
                             // the leader's full barrier counts both CTAs' bytes
-                            if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                            if (leader) um::mbar_arrive_expect_tx(&full[stage], 2 * (kABytes + kBRows * 128));
                             const uint32_t bar = leader ? fb : um::mapa(fb, 0);
                             if (MODE == M_P && a.fused_gate) {
                                 // [4 groups][W_c1, W_c2][16 rows] in one box
@@ -319,7 +335,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             } else {
                                 um::tma_load_3d_pair(sa, mA, bar, kx, ay, az);
                             }
-                            um::tma_load_3d_pair(sa + kABytes, &tmB, bar, kx, by, bz);
+                            if (kSkip) um::tma_load_4d_pair(sa + kABytes, &tmB, bar, kx, 1, by / (kSkip ? kG : 1), bz);
+                            else um::tma_load_3d_pair(sa + kABytes, &tmB, bar, kx, by, bz);
                             if (++stage == S) { stage = 0; ph ^= 1u; }
                         }
                     }
@@ -353,7 +370,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     um::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
                     // distance tiles: only the references the tile's rows can see
-                    const uint32_t id = MODE == M_DIST ? um::idesc_bf16_f32(2 * kBM, dist_cols(a, it.t, n)) : kIdesc;
+                    const uint32_t id = MODE == M_DIST ? um::idesc_bf16_f32(2 * kBM, dist_cols(a, it.t, n))
+                                                       : um::idesc_bf16_f32(2 * kBM, 2 * kBRows);
                     for (int kc = 0; kc < k_iters; ++kc) {
                         if (!um::mbar_wait(&full[stage], ph, a.wait_cycles)) {
                             ok = false;
@@ -469,13 +487,15 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 // rows (unused places point at the all-zero row), 1/k and a live flag,
                 // prepared in shared memory while the accumulator fills
                 int4 *info = info_buf + (warp - 2) * 128;
-                const int own0 = h * kHalfN + (q < 2 ? 0 : 64);
+                const int tok0 = it.t * 2 * kBM + h * kHalfN + (q < 2 ? 0 : 64);
                 const int zoff = a.LB * a.n_ref * a.d_ff;
                 const int lboff = it.lb * a.n_ref;
                 __syncwarp();
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    const int tj = it.t * 2 * kBM + own0 + cc * 32 + lane;
+                    const int j = cc * 32 + lane;
+                    if (j >= kBRows / 2) continue;         // a skip layout has fewer than 64
+                    const int tj = tok0 + s1_token<kSkip ? kG : 0>(j);
                     int rs = 0, cf = 1;
                     int4 ix = make_int4(-1, -1, -1, -1);
                     if (tj < a.rows) {
@@ -494,10 +514,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
                         live = 1.0f;
                     }
-                    info[2 * (cc * 32 + lane)] = o;
+                    info[2 * j] = o;
                     // 1/k for a live token (0 when its pool is empty), -1 for a reference
                     // token or an exact copy (dh = 0)
-                    info[2 * (cc * 32 + lane) + 1] = make_int4(__float_as_int(live > 0.0f ? inv_k : -1.0f), 0, 0, 0);
+                    info[2 * j + 1] = make_int4(__float_as_int(live > 0.0f ? inv_k : -1.0f), 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -590,8 +610,12 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const int f = n * kBM + (int)rank * (kBM / 2) + (q & 1) * 32 + lane;
                     const bool fok = f < a.d_ff;
                     const float2 *P12f = (const float2 *)a.P12 + (fok ? f : 0);
-                    const int own0 = h * kHalfN + (gate ? 0 : 64);
-                    const int give0 = h * kHalfN + (gate ? 64 : 0);
+                    // this warp's own accumulator columns and those it hands over; both
+                    // warps of the pair hold kBRows / 2 tokens
+                    constexpr int kOwn = kBRows / 2;
+                    const int own0 = h * kBRows + (gate ? 0 : kOwn);
+                    const int give0 = h * kBRows + (gate ? kOwn : 0);
+                    const int tok0 = it.t * 2 * kBM + h * kHalfN + (gate ? 0 : 64);
                     const int4 *info = info_buf + (warp - 2) * 128;
                     const int gb = 2 + 4 * h;                     // first warp of this half
                     const int me = warp - 2, partner = gb + ((warp - gb) ^ 2) - 2;
@@ -619,11 +643,12 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // has scale -1, so dh = 0.
                     auto finish = [&](int c, const float (&v)[kXTok], int v0, const float *xr,
                                       const float2 (&pr)[kS1Round][4], const float (&sc)[kS1Round]) {
-                        const int t0 = it.t * 2 * kBM + own0 + c;
-                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
-                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + t0) * a.d_ff + f;
+                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + tok0) * a.d_ff + f;
+                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + tok0) * a.d_ff + f;
 #pragma unroll
                         for (int u = 0; u < kS1Round; ++u) {
+                            constexpr int kGs = kSkip ? kG : 0;
+                            const int tu = s1_token<kGs>(c + u);   // a constant once unrolled
                             const float pv = xr[(v0 + u) * 32 + lane];
                             const float g1 = gate ? v[v0 + u] : pv, g2 = gate ? pv : v[v0 + u];
                             const float2 s01 = __fadd2_rn(pr[u][0], pr[u][1]);
@@ -640,16 +665,16 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const float live = sc[u] >= 0.0f ? 1.0f : 0.0f;
                             const float dh = num * rcp_fast(d.x * d.y) * live;
                             const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
-                            if (fok && t0 + u < a.rows) {
-                                hi[(size_t)u * a.d_ff] = hb;
-                                lo[(size_t)u * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                            if (fok && tok0 + tu < a.rows) {
+                                hi[(size_t)tu * a.d_ff] = hb;
+                                lo[(size_t)tu * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
                             }
                         }
                     };
                     gather(0, pr3[0], sc3[0]);
                     gather(kS1Round, pr3[1], sc3[1]);
 #pragma unroll
-                    for (int c = 0; c < 64; c += kXTok) {
+                    for (int c = 0; c < kOwn; c += kXTok) {
                         // double-buffered: a buffer is rewritten only after the next
                         // exchange barrier, which the partner reaches after reading it
                         float *xw = xbuf + (size_t)(((xcnt & 1u) * kEpiWarps + me) * kXTok) * 32;
@@ -665,9 +690,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         float v[kXTok];
                         um::tmem_ld8(tb + own0 + c, v);
                         const int r0 = c / kS1Round;       // rounds r0 and r0 + 1 of this exchange
-                        if (c + 2 * kS1Round < 64) gather(c + 2 * kS1Round, pr3[(r0 + 2) % 3], sc3[(r0 + 2) % 3]);
+                        if (c + 2 * kS1Round < kOwn) gather(c + 2 * kS1Round, pr3[(r0 + 2) % 3], sc3[(r0 + 2) % 3]);
                         finish(c, v, 0, xr, pr3[r0 % 3], sc3[r0 % 3]);
-                        if (c + 3 * kS1Round < 64) gather(c + 3 * kS1Round, pr3[(r0 + 3) % 3], sc3[(r0 + 3) % 3]);
+                        if (c + 3 * kS1Round < kOwn) gather(c + 3 * kS1Round, pr3[(r0 + 3) % 3], sc3[(r0 + 3) % 3]);
                         finish(c + kS1Round, v, kS1Round, xr, pr3[(r0 + 1) % 3], sc3[(r0 + 1) % 3]);
                     }
                 } else {  // M_S2
@@ -791,6 +816,24 @@ bool make_map_store(CUtensorMap *m, const void *base, uint64_t inner, uint64_t r
     return r == CUDA_SUCCESS;
 }
 
+// bf16 token rows [batch][rows][inner] as [batch][rows / g][g][inner] (rows % g == 0):
+// box = 64 (inner) x rows 1..g-1 of a group x 128 / g groups, 128-byte swizzle; the box
+// lands as 128 (g - 1) / g consecutive 128-byte rows.
+static bool make_map_skip(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                          uint64_t batch, int g)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {inner, (cuuint64_t)g, rows / g, batch};
+    cuuint64_t strides[3] = {inner * 2, inner * 2 * g, inner * 2 * rows};
+    cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)(g - 1), (cuuint32_t)(kHalfN / g), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // W_c1 and W_c2 ([L][d_ff][W] each, i.e. [L*d_ff][W]) seen as one [2][L*d_ff][W] tensor
 // whose matrix stride is the distance between them: box = 64 (inner) x 64 rows x both
 // matrices, i.e. 64 rows of W_c1 followed by the same 64 rows of W_c2.
@@ -827,11 +870,11 @@ static bool make_map_gates16(CUtensorMap *m, const void *W1, long long gate_off,
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, int kG = 0>
 static cudaError_t run(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                        const UmmaArgs &args, cudaStream_t s)
 {
-    auto kern = k_umma<MODE>;
+    auto kern = k_umma<MODE, kG>;
     constexpr int smem = Cfg<MODE>::kSmem;
     const long long items = (long long)args.LB * args.tiles_t * args.tiles_n;
     if (items <= 0) return cudaSuccess;
@@ -961,7 +1004,16 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
         UmmaArgs p = a;
         p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = ff_slices;
         p.k_chunks = kw; p.a_sources = 1;
-        if ((e = run<M_S1>(mG1, mW2, mX, p, s)) != cudaSuccess) return e;
+        // a fixed schedule from position 0 whose stride divides 8 makes every
+        // position 0 mod 8 a reference: those rows are left out of the MMA
+        const bool skip8 = g.alpha == 0.0 && g.first == 0 && g.stride >= 1 && 8 % g.stride == 0 &&
+                           g.T % 8 == 0;
+        CUtensorMap mXs;
+        if (skip8 && make_map_skip(&mXs, kv, g.W, g.T, g.LB, 8)) {
+            if ((e = run<M_S1, 8>(mG1, mW2, mXs, p, s)) != cudaSuccess) return e;
+        } else if ((e = run<M_S1>(mG1, mW2, mX, p, s)) != cudaSuccess) {
+            return e;
+        }
     }
     {
         UmmaArgs p = a;

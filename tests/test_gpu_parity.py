@@ -101,9 +101,13 @@ def test_gate_weight_placement_gives_identical_records():
 
 def test_edge_cases_small_T_first_offset_k():
     base = C["llama3.1-8b-kv"].replace(L=1, N=2, D=64, d_ff=256, d_c=64)
+    # T % 8 == 0 with a stride dividing 8 from position 0 takes the layout that leaves
+    # the reference rows out of the first compressor layer: one group, a ragged tile,
+    # references at every 4th and every 2nd position
     for cfg in (base.replace(T=1), base.replace(T=9), base.replace(T=130),
                 base.replace(T=300, first=5), base.replace(T=300, k=1),
-                base.replace(T=300, k=2, bits=2)):
+                base.replace(T=300, k=2, bits=2), base.replace(T=8), base.replace(T=136),
+                base.replace(T=512, stride=4), base.replace(T=264, stride=2)):
         bufs, kv, w, gpu, rep = _parity(cfg, n_sample=cfg.T)
         if cfg.first > 0:
             # tokens before the first reference have an empty pool: no refs, z = f_c(kv)
