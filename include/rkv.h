@@ -185,7 +185,11 @@ rkv_status rkv_restore_kv(const rkv_params *p, const rkv_ref_pool *pool, const r
  * query head j reading key/value head floor(j / (H/N)) (grouped heads; the page writes
  * the formula per head).  I = the rows n < n_sel of k_hat/v_hat whose sel[lb][n] is a
  * position in [0, T) (padding and out-of-range entries, zero rows of rkv_restore_kv,
- * are left out); an empty I gives zeros.  Scores, softmax and sums in fp32.
+ * are left out); an empty I gives zeros.  Softmax and sums in fp32; for D = 128 the
+ * scores and the weighted sums of V^ run on the tensor cores (bf16 q, K^, V^ with fp32
+ * accumulation; the probabilities enter as a bf16 hi + lo pair, relative error about
+ * 2^-16), other D on CUDA cores in fp32.  On the tensor-core path a device wait that runs
+ * out (about a second) leaves NaN in the affected head's outputs.
  * q: bf16 [L*B][H][D]; k_hat, v_hat: bf16 [L*B][n_sel][N D] (rkv_restore_kv's
  * outputs); sel: as given to rkv_restore_kv; out: fp32 [L*B][H][D].
  * workspace: >= the bytes rkv_attention_workspace reports (per-split partials).

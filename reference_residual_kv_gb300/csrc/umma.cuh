@@ -133,6 +133,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major, shape M x N.
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)   bits 10-12 B format (1 = bf16)
 //   bit 15/16 A/B major (0 = K)   bits 17-22 N >> 3             bits 24-28 M >> 4
+// The same for an MN-major operand with 128-byte swizzle: 1024-B atoms of 8 K rows x 64
+// MN elements (one 128-B row per K index); `lbo` = byte distance between atoms along MN,
+// `sbo` = byte distance between 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
