@@ -80,6 +80,7 @@ struct UmmaArgs {
     int k_chunks, a_sources;
     int fused_gate;       // M_P/M_S1: tmA0 maps W_c1 and W_c2 together (one box per stage)
     int W, d_ff, d_c, n_ref, bits;
+    int dh_rows;          // rows of dh per lb: T, or the non-reference count when compacted
     float *P12;           // [LB * n_ref + 1][d_ff] of {x.W_c1[f], x.W_c2[f]} per reference
     const float *ref_sqnorm;
     const int32_t *pool_size, *ref_slot;
@@ -195,11 +196,16 @@ __device__ __forceinline__ float silu_fast(float u)
     return __fdividef(u, 1.0f + __expf(-u));
 }
 
-// S1 with kG > 0: every position that is 0 mod kG is a reference (fixed stride dividing
-// kG, first reference at 0), where dh = 0.  Those token rows are not loaded: tmB is then
-// a [LB][T/kG][kG][W] view, each CTA's B half holds rows 1..kG-1 of its 128/kG groups
-// (kBRows rows), and the MMA's N is 2 kBRows.  TMEM column j of half h is token
-// h*128 + (j / (kG-1)) kG + j % (kG-1) + 1 of the tile.
+// kG > 0: every position that is 0 mod kG is a reference (fixed stride dividing kG,
+// first reference at 0), where dh = 0 and the record is all zero.
+//   S1: those token rows are not loaded: tmB is then a [LB][T/kG][kG][W] view, each CTA's
+//       B half holds rows 1..kG-1 of its 128/kG groups (kBRows rows), and the MMA's N is
+//       2 kBRows.  TMEM column j of half h is token h*128 + (j / (kG-1)) kG + j % (kG-1)
+//       + 1 of the tile.  dh is stored compacted: row c of [LB][T (kG-1)/kG][d_ff] is the
+//       c-th non-reference position, so a warp's tokens are consecutive rows.
+//   S2: runs over the compacted rows (a.rows of them); row c is token
+//       (c / (kG-1)) kG + c % (kG-1) + 1, and the row that opens a group also writes the
+//       all-zero record of the group's reference token.
 template <int MODE, int kG>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -208,6 +214,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     using C = Cfg<MODE>;
     constexpr int S = C::kStages;
     constexpr bool kSkip = MODE == M_S1 && kG > 0;
+    constexpr bool kCompact = MODE == M_S2 && kG > 0;
     constexpr int kBRows = kSkip ? kHalfN * (kG - 1) / kG : kHalfN;
     static_assert(!kSkip || (kHalfN % (kSkip ? kG : 1) == 0 && (kBRows / 2) % kXTok == 0 && kBRows % 8 == 0),
                   "skip layout: whole groups per CTA, whole exchanges per warp");
@@ -470,6 +477,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             if (!item_get<MODE>(a, i, it)) continue;
             const int r = it.t * 2 * kBM + (int)rank * kBM + row;   // token row (M_DIST, M_S2)
             const bool in = r < a.rows;
+            // M_S2 over compacted rows: the token of row r
+            const int tokr = kCompact ? (r / (kCompact ? kG - 1 : 1)) * kG + r % (kCompact ? kG - 1 : 1) + 1 : r;
 
             float be[kList];
             int bs[kList];
@@ -481,7 +490,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 tile_pool = a.pool_size[min(a.T, (it.t + 1) * 2 * kBM) - 1];
             }
             bool is_ref = true;
-            if (MODE == M_S2) is_ref = in ? (a.ref_slot[r] >= 0) : true;
+            if (MODE == M_S2) is_ref = in ? (a.ref_slot[tokr] >= 0) : true;
             if (MODE == M_S1) {
                 // this warp's 64 tokens: row offsets of the chosen references' projection
                 // rows (unused places point at the all-zero row), 1/k and a live flag,
@@ -616,6 +625,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const int own0 = h * kBRows + (gate ? 0 : kOwn);
                     const int give0 = h * kBRows + (gate ? kOwn : 0);
                     const int tok0 = it.t * 2 * kBM + h * kHalfN + (gate ? 0 : 64);
+                    // dh row of this warp's first token (compacted when reference rows are
+                    // left out: the warp's tokens are then consecutive rows)
+                    const int drow0 = kSkip ? it.t * 2 * kBRows + own0 : tok0;
                     const int4 *info = info_buf + (warp - 2) * 128;
                     const int gb = 2 + 4 * h;                     // first warp of this half
                     const int me = warp - 2, partner = gb + ((warp - gb) ^ 2) - 2;
@@ -643,12 +655,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // has scale -1, so dh = 0.
                     auto finish = [&](int c, const float (&v)[kXTok], int v0, const float *xr,
                                       const float2 (&pr)[kS1Round][4], const float (&sc)[kS1Round]) {
-                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.T + tok0) * a.d_ff + f;
-                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.T + tok0) * a.d_ff + f;
+                        __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.dh_rows + drow0) * a.d_ff + f;
+                        __nv_bfloat16 *lo = a.dh_lo + ((size_t)it.lb * a.dh_rows + drow0) * a.d_ff + f;
 #pragma unroll
                         for (int u = 0; u < kS1Round; ++u) {
-                            constexpr int kGs = kSkip ? kG : 0;
-                            const int tu = s1_token<kGs>(c + u);   // a constant once unrolled
                             const float pv = xr[(v0 + u) * 32 + lane];
                             const float g1 = gate ? v[v0 + u] : pv, g2 = gate ? pv : v[v0 + u];
                             const float2 s01 = __fadd2_rn(pr[u][0], pr[u][1]);
@@ -665,9 +675,9 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const float live = sc[u] >= 0.0f ? 1.0f : 0.0f;
                             const float dh = num * rcp_fast(d.x * d.y) * live;
                             const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
-                            if (fok && tok0 + tu < a.rows) {
-                                hi[(size_t)tu * a.d_ff] = hb;
-                                lo[(size_t)tu * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
+                            if (fok && drow0 + c + u < a.dh_rows) {
+                                hi[(size_t)(c + u) * a.d_ff] = hb;
+                                lo[(size_t)(c + u) * a.d_ff] = __float2bfloat16_rn(dh - __bfloat162float(hb));
                             }
                         }
                     };
@@ -710,9 +720,10 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         uint32_t wq[4];
                         float zmin, delta;
                         quant_group32(v, a.bits, wq, zmin, delta);
-                        const size_t rec = (size_t)it.lb * a.T + r;
+                        const size_t rec = (size_t)it.lb * a.T + tokr;
                         const int g = c0 >> 5;
-                        uint8_t *dst = a.codes + rec * (size_t)(a.d_c * a.bits / 8) + g * (a.bits * 4);
+                        const size_t cpitch = (size_t)(a.d_c * a.bits / 8);
+                        uint8_t *dst = a.codes + rec * cpitch + g * (a.bits * 4);
                         if (a.bits == 4) *(uint4 *)dst = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                         else *(uint2 *)dst = make_uint2(wq[0], wq[1]);
                         a.hdr[rec * (a.d_c / 32) + g] = make_float2(zmin, delta);
@@ -721,6 +732,18 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 zo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                        if (kCompact && r % (kCompact ? kG - 1 : 1) == 0) {
+                            // the group's reference token, just before this one: zero record
+                            uint8_t *dr = dst - cpitch;
+                            if (a.bits == 4) *(uint4 *)dr = make_uint4(0u, 0u, 0u, 0u);
+                            else *(uint2 *)dr = make_uint2(0u, 0u);
+                            a.hdr[(rec - 1) * (a.d_c / 32) + g] = make_float2(0.0f, 0.0f);
+                            if (a.z_out) {
+                                float4 *zo = (float4 *)(a.z_out + (rec - 1) * a.d_c + c0);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) zo[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            }
                         }
                     }
                 }
@@ -946,6 +969,7 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     a.copy_flag = copy_flag;
     a.dh_hi = dh_hi; a.dh_lo = dh_lo; a.codes = cache->codes; a.hdr = (float2 *)cache->hdr;
     a.z_out = z_out; a.status = status;
+    a.dh_rows = g.T;
     const int kw = (g.W + kBK - 1) / kBK;
     const int ff_slices = (g.d_ff + kBM - 1) / kBM;
     // W_c2 at a 16-byte multiple after W_c1 (e.g. both in one allocation): the two gate
@@ -1000,16 +1024,21 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
                                   copy_flag, scan_list, scan_list + (size_t)g.LB * g.T, rr_list,
                                   (int32_t *)(rr_list + (size_t)g.LB * g.T), status, s)) != cudaSuccess)
         return e;
+    // a fixed schedule from position 0 whose stride divides 8 makes every position 0 mod 8
+    // a reference: those rows are left out of S1's MMA, and dh holds only the other 7 of
+    // every 8 positions, which S2 then runs over
+    const bool skip8 = g.alpha == 0.0 && g.first == 0 && g.stride >= 1 && 8 % g.stride == 0 &&
+                       g.T % 8 == 0;
+    CUtensorMap mXs, mHc, mLc;
+    const int Tc = g.T / 8 * 7;
+    const bool compact = skip8 && make_map_skip(&mXs, kv, g.W, g.T, g.LB, 8) &&
+                         make_map(&mHc, dh_hi, g.d_ff, Tc, g.LB, kBM) && make_map(&mLc, dh_lo, g.d_ff, Tc, g.LB, kBM);
     {
         UmmaArgs p = a;
         p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = ff_slices;
         p.k_chunks = kw; p.a_sources = 1;
-        // a fixed schedule from position 0 whose stride divides 8 makes every
-        // position 0 mod 8 a reference: those rows are left out of the MMA
-        const bool skip8 = g.alpha == 0.0 && g.first == 0 && g.stride >= 1 && 8 % g.stride == 0 &&
-                           g.T % 8 == 0;
-        CUtensorMap mXs;
-        if (skip8 && make_map_skip(&mXs, kv, g.W, g.T, g.LB, 8)) {
+        if (compact) {
+            p.dh_rows = Tc;
             if ((e = run<M_S1, 8>(mG1, mW2, mXs, p, s)) != cudaSuccess) return e;
         } else if ((e = run<M_S1>(mG1, mW2, mX, p, s)) != cudaSuccess) {
             return e;
@@ -1017,7 +1046,9 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
     }
     {
         UmmaArgs p = a;
-        p.rows = g.T; p.tiles_t = g.n_mtiles; p.tiles_n = (g.d_c + kBN - 1) / kBN;
+        p.rows = compact ? Tc : g.T;
+        p.tiles_t = (p.rows + kTileM - 1) / kTileM;
+        p.tiles_n = (g.d_c + kBN - 1) / kBN;
         p.k_chunks = (g.d_ff + kBK - 1) / kBK; p.a_sources = 2;
         const long long fc = g_fault_cycles.exchange(0);
         const int fs = g_fault_skip.exchange(-1);
@@ -1025,7 +1056,11 @@ cudaError_t launch_umma_compress(const Geometry &g, const void *kv, const rkv_re
             p.wait_cycles = fc;
             p.skip_use = fs;
         }
-        if ((e = run<M_S2>(mHi, mLo, mW3, p, s)) != cudaSuccess) return e;
+        if (compact) {
+            if ((e = run<M_S2, 8>(mHc, mLc, mW3, p, s)) != cudaSuccess) return e;
+        } else if ((e = run<M_S2>(mHi, mLo, mW3, p, s)) != cudaSuccess) {
+            return e;
+        }
     }
     return cudaSuccess;
 }
