@@ -11,7 +11,7 @@
 //   warp 1      TMEM allocation (both CTAs, 512 columns = two 256-column
 //               accumulators); MMA issue (leader only)
 //   warps 2..9  epilogue: TMEM lane quarter q = warp % 4, column half h
-//   warps 10..13 (M_DIST only) ||x||^2 of every token row, read from the token
+//   warps 10, 11, 14, 15 (M_DIST only) ||x||^2 of every token row, read from the token
 //               tiles in shared memory on each token tile's first N tile while the
 //               MMA works; a stage is free once the MMA and these warps are done
 //               with it (the top-k finalisation's distance bound needs the norms)
@@ -55,7 +55,10 @@ constexpr int kStageBytes = kABytes + kBBytes;   // per CTA
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kNormWarps = 4;                    // M_DIST: token-norm warps per CTA
-template <int MODE> constexpr int threads_of() { return kThreads + (MODE == M_DIST ? 32 * kNormWarps : 0); }
+// M_DIST launches warps 10..15 and runs the norm warps as 10, 11, 14 and 15 (schedulers 2
+// and 3): warps 12 and 13 would share schedulers 0 and 1 with the single producer and MMA
+// threads, so they stay idle
+template <int MODE> constexpr int threads_of() { return kThreads + (MODE == M_DIST ? 32 * (kNormWarps + 2) : 0); }
 constexpr int kInfoBytes = kEpiWarps * 64 * 32;  // S1: 64 tokens x 32 B per epilogue warp
 constexpr int kS1Round = 4;                      // S1: tokens per round of gathers (one round ahead)
 constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
@@ -407,6 +410,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             um::mma2_commit_mc(drain, 1);
             um::mbar_wait(drain, 0, a.wait_cycles);
         }
+    } else if (MODE == M_DIST && warp >= 2 + kEpiWarps && (warp & 3) < 2) {
+        // idle (see threads_of)
     } else if (MODE == M_DIST && warp >= 2 + kEpiWarps) {
         // ------------------------------------------------------------ token norms
         // Every stage use, in the producer's order: wait until its copies have landed
@@ -416,7 +421,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         // warp w owns token row 32w + l of this CTA's 128 A rows; a stage holds 64 of
         // its values (one 128-byte row, 16-byte chunk c at position c ^ (row % 8), the
         // 128-byte swizzle).  ||x||^2 is a sum over stages of per-stage sums of squares.
-        const int nrow = (warp - 2 - kEpiWarps) * 32 + lane;
+        const int nrow = (warp < 12 ? warp - 10 : warp - 12) * 32 + lane;
         int stage = 0;
         uint32_t ph = 0;
         bool ok = true;

@@ -41,6 +41,11 @@ def _attend(cfg, q_bits, k_bits, v_bits, sel):
     ("llama3.1-8b-kv", 333, dict(N=16, D=64)),         # D = 64, groups of 2
     ("llama3.1-8b-kv", 517, dict(N=4, D=64)),          # D = 64, groups of 8
     ("llama3.1-8b-kv", 901, dict(N=4, D=256, H=16)),   # D = 256, groups of 4
+    # D = 128 takes the tensor-core pass: one query head per KV head, groups of 2 and 8,
+    # and selections one row short of, one row past and just under whole 128-row tiles
+    ("llama3.1-8b-kv", 127, dict(H=8)),
+    ("llama3.1-8b-kv", 129, dict(H=16)),
+    ("llama3.1-8b-kv", 255, dict(H=64)),
 ])
 def test_attention_matches_oracle(name, n_sel, shape):
     cfg = C[name].replace(L=2, T=4096, **shape)
