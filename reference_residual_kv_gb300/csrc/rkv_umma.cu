@@ -582,15 +582,28 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         // the columns whose expansion is below this row's current last
                         // entry (a superset of those that will enter: the bound only falls),
                         // collected in four independent partial masks
-                        const float thr = be[kList - 1];
+                        float thr = be[kList - 1];
                         const int lim = pool - s0;           // columns j < lim are in the pool
-                        uint32_t hm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const float rj = __shfl_sync(0xffffffffu, rnv[cc], j);
                             v[j] = fmaf(-2.0f, v[j], rj);
-                            hm[j & 3] |= (uint32_t)(j < lim && v[j] < thr) << j;
                         }
+                        // a row's first full chunk (empty list): instead of +inf, the largest
+                        // of the eight 4-column minima, which is at or above the chunk's 8th
+                        // smallest value (eight values lie at or below it), so no column that
+                        // belongs in the list is left out and about half the columns are
+                        const bool seed = thr == INFINITY && lim >= 32;
+                        if (__any_sync(0xffffffffu, seed)) {
+                            float mx = -INFINITY;
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                mx = fmaxf(mx, fminf(fminf(v[4 * g], v[4 * g + 1]), fminf(v[4 * g + 2], v[4 * g + 3])));
+                            if (seed) thr = nextafterf(mx, INFINITY);
+                        }
+                        uint32_t hm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) hm[j & 3] |= (uint32_t)(j < lim && v[j] < thr) << j;
                         uint32_t hit = (hm[0] | hm[1]) | (hm[2] | hm[3]);
                         // each lane inserts only its own hits, in increasing column order
                         // (strict < keeps the lower slot ahead of an equal later one).  The
