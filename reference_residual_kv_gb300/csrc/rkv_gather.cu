@@ -80,9 +80,10 @@ template <> struct RefLoad<uint8_t> {     // FP8 E4M3: exact in fp16, two per co
 // Launch shape by reference dtype (measured): bf16 and fp32 references run persistent
 // warps, 3 blocks per SM, each warp walking several tokens with the next token's record
 // loaded ahead; FP8 references (half the bytes per reference, more conversions) run one
-// warp per token at 5 blocks per SM with four mean steps' loads in flight.
+// warp per token at 4 blocks per SM (64 registers) with four mean steps' loads in flight
+// (a sweep of 2..8 blocks and 2..8 steps: 4 and 4 fastest, 4 % ahead of 5 and 4).
 template <typename RefT> constexpr bool kPersistent = sizeof(RefT) != 1;
-template <typename RefT> constexpr int kGatherBlocks = kPersistent<RefT> ? 3 : 5;
+template <typename RefT> constexpr int kGatherBlocks = kPersistent<RefT> ? 3 : 4;
 
 template <typename OutT>
 __device__ __forceinline__ void store8(OutT *dst, const float (&v)[8]);
