@@ -131,7 +131,6 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
               int2 *__restrict__ rr_list, int32_t *__restrict__ rr_count)
 {
     enum { kNone = 0, kDone, kRerank, kCopyCheck, kFull };
-    const int lane = threadIdx.x & 31;
     const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     int state = kNone, lb = 0, nlists = 0;
     int ch[kMaxK] = {kNoSlot, kNoSlot, kNoSlot, kNoSlot};
@@ -175,11 +174,11 @@ k_topk_select(const T *__restrict__ kv, const T *__restrict__ refs,
 #pragma unroll
             for (int j = 0; j <= kMaxK; ++j) { te[j] = INFINITY; ts[j] = kNoSlot; }
             float e_last = INFINITY;   // smallest last entry of a full list
-            for (int ch = 0; ch < nch; ++ch) {
+            for (int item = 0; item < nch; ++item) {
                 // the work item's two sorted lists, all their float4 loads in flight at once
                 float4 e4[kCand / 2];
 #pragma unroll
-                for (int j = 0; j < kCand / 2; ++j) e4[j] = cp[ch * (kCand / 2) + j];
+                for (int j = 0; j < kCand / 2; ++j) e4[j] = cp[item * (kCand / 2) + j];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float4 tail = e4[h * (kList / 2) + kList / 2 - 1];
