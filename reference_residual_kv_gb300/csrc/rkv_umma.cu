@@ -64,12 +64,13 @@ constexpr int kS1Round = 4;                      // S1: tokens per round of gath
 constexpr int kXTok = 8;                         // S1: tokens per exchange between warp pairs
 constexpr int kXBytes = 2 * kEpiWarps * kXTok * 32 * 4;   // double-buffered exchange
 constexpr int kGateRows = 16;                    // M_P: W_c1 rows, then the same W_c2 rows, per lane quarter
+constexpr int kDistVBytes = kEpiWarps * 32 * 32 * 4;   // M_DIST: each epilogue lane's 32 expansion values
 constexpr uint16_t kPairMask = 3;
 
 template <int MODE> struct Cfg {
     static constexpr bool kT = MODE == M_P || MODE == M_S1;   // transposed
     static constexpr int kStages = MODE == M_S1 || MODE == M_DIST ? 6 : 7;
-    static constexpr int kExtra = MODE == M_S1 ? kInfoBytes + kXBytes : 0;
+    static constexpr int kExtra = MODE == M_S1 ? kInfoBytes + kXBytes : (MODE == M_DIST ? kDistVBytes : 0);
     static constexpr int kSmem = kStages * kStageBytes + 1024 + 256 + kExtra;
     static_assert(kSmem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
     static_assert((3 * kStages + 5) * 8 + 8 <= 256, "barriers overflow their 256-byte block");
@@ -154,31 +155,6 @@ __device__ __forceinline__ int dist_cols(const UmmaArgs &a, int t, int n)
     return own >= kBN ? kBN : ((own + 31) & ~31);
 }
 
-// v[j] for a lane-dependent j in [0, 32), by a tree of selects: indexing the register
-// array with a runtime j would put it in local memory
-__device__ __forceinline__ float pick32(const float (&v)[32], int j)
-{
-    float a[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a[i] = (j & 16) ? v[i + 16] : v[i];
-    float b[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = (j & 8) ? a[i + 8] : a[i];
-    float c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[i + 4] : b[i];
-    const float d0 = (j & 2) ? c[2] : c[0], d1 = (j & 2) ? c[3] : c[1];
-    return (j & 1) ? d1 : d0;
-}
-
-// S1: offset, from the warp's first token, of the token in its j-th own accumulator
-// column; with reference rows skipped (kG > 0) a column group of kG - 1 covers kG tokens
-template <int kG>
-__host__ __device__ constexpr int s1_token(int j)
-{
-    return kG > 0 ? (j / (kG - 1)) * kG + j % (kG - 1) + 1 : j;
-}
-
 // 2^x and 1/x by the approximate hardware instructions (relative error ~2^-22)
 __device__ __forceinline__ float exp2f_fast(float x)
 {
@@ -233,6 +209,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     int4 *info_buf = (int4 *)(tiles + S * kStageBytes + 256);
     float *xbuf = (float *)(tiles + S * kStageBytes + 256 + kInfoBytes);
+    float *dvbuf = (float *)(tiles + S * kStageBytes + 256);   // M_DIST
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = um::cluster_rank();
@@ -612,9 +589,21 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         // a hit that no longer beats the last entry passes through
                         // unchanged.
                         const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)__popc(hit));
+                        // the chunk's values go to this lane's row of shared memory (16-byte
+                        // unit u of lane l at u ^ (l % 8)), so that a round reads its
+                        // candidate with one indexed load
+                        float *vrow = dvbuf + ((warp - 2) * 32 + lane) * 32;
+                        if (rounds > 0) {
+                            __syncwarp();                    // the previous chunk's reads are done
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                *(float4 *)(vrow + ((u ^ (lane & 7)) << 2)) =
+                                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                            __syncwarp();
+                        }
                         for (int rd = 0; rd < rounds; ++rd) {
                             const int j = __ffs(hit) - 1;
-                            float ce = hit ? pick32(v, j) : INFINITY;
+                            float ce = hit ? vrow[(((j >> 2) ^ (lane & 7)) << 2) | (j & 3)] : INFINITY;
                             hit &= hit - 1u;
                             int cs = s0 + j;
 #pragma unroll
