@@ -155,6 +155,14 @@ __device__ __forceinline__ int dist_cols(const UmmaArgs &a, int t, int n)
     return own >= kBN ? kBN : ((own + 31) & ~31);
 }
 
+// S1: offset, from the warp's first token, of the token in its j-th own accumulator
+// column; with reference rows skipped (kG > 0) a column group of kG - 1 covers kG tokens
+template <int kG>
+__host__ __device__ constexpr int s1_token(int j)
+{
+    return kG > 0 ? (j / (kG - 1)) * kG + j % (kG - 1) + 1 : j;
+}
+
 // 2^x and 1/x by the approximate hardware instructions (relative error ~2^-22)
 __device__ __forceinline__ float exp2f_fast(float x)
 {
