@@ -184,14 +184,27 @@ __device__ __forceinline__ float silu(float u)
 // clamped to [0, 2^b - 1]; max == min stores the constant with delta = 0, q = 0.
 // Packs INT4 as 4 words (coordinate 2j low nibble of byte j) and INT2 as 2 words
 // (coordinate 4j+i in bits 2i..2i+1 of byte j).
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, uint32_t (&w)[4],
                                               float &zmin, float &delta)
 {
-    float lo = v[0], hi = v[0];
+    // extremes by three-input min/max: a chain of 15 steps per extreme
+    float lo = fminf(v[0], v[1]), hi = fmaxf(v[0], v[1]);
 #pragma unroll
-    for (int j = 1; j < 32; ++j) {
-        lo = fminf(lo, v[j]);
-        hi = fmaxf(hi, v[j]);
+    for (int j = 2; j < 32; j += 2) {
+        lo = min3f(lo, v[j], v[j + 1]);
+        hi = max3f(hi, v[j], v[j + 1]);
     }
     const int qmax = (1 << bits) - 1;
     zmin = lo;
@@ -202,24 +215,29 @@ __device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, ui
     }
     const float dl = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
     delta = dl;
-    // u = RN(RN((v - lo)/delta) + 1/2) < 16 is first estimated with RN(1/delta) and a
-    // multiplication: the estimate lies within 2^-18 of u (two relative roundings of
-    // 2^-24 on a quotient <= 15, plus half-ulp roundings <= 2^-21 each), so floor can
-    // differ only where the estimate is within 2^-17 of an integer; there (and where
-    // delta is too small for a finite reciprocal) the correctly rounded division is
-    // used.
+    // q = floor(RN(RN(d/delta) + 1/2)) with d = v - lo in [0, hi - lo].  It is first
+    // estimated from x = d RN(1/delta), rounded to the nearest integer inside the same
+    // FMA (adding 1.5 2^23 leaves round(x) in the low mantissa bits), and r = x - round(x)
+    // from one more FMA.  x lies within 2^-19 of RN(d/delta) (RN(1/delta) is within
+    // 2^-24 relative and the quotient is at most 15, within 2^-20 of its rounding); so
+    // where |r| is at least 2^-17 short of 1/2, RN(d/delta) is more than 2^-18 away from
+    // the half-integer where floor(. + 1/2) changes, the rounding of RN(d/delta) + 1/2
+    // (at most 2^-20) cannot cross it, and q = round(x).  Nearer than that (and where
+    // delta is too small for a finite reciprocal) the correctly rounded division decides.
     const float rdl = __frcp_rn(dl);
     const bool fast = dl >= 0x1p-100f;
+    constexpr float kMagic = 12582912.0f;     // 1.5 * 2^23
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const float d = __fsub_rn(v[j], lo);
-        float u = __fadd_rn(__fmul_rn(d, rdl), 0.5f);
-        float fu = floorf(u);
-        if (!fast || __fsub_rn(u, fu) < 0x1p-17f || __fsub_rn(u, fu) > 1.0f - 0x1p-17f) {
-            u = __fadd_rn(__fdiv_rn(d, dl), 0.5f);
-            fu = floorf(u);
+        const float t = __fmaf_rn(d, rdl, kMagic);
+        const float qf = __fsub_rn(t, kMagic);                 // round(x), exact
+        const float r = __fmaf_rn(d, rdl, -qf);
+        int q = __float_as_int(t) - __float_as_int(kMagic);
+        if (!fast || fabsf(r) > 0.5f - 0x1p-17f) {
+            const float u = __fadd_rn(__fdiv_rn(d, dl), 0.5f);
+            q = (int)floorf(u);
         }
-        int q = (int)fu;
         q = q < 0 ? 0 : (q > qmax ? qmax : q);
         if (bits == 4)
             w[j >> 3] |= (uint32_t)q << (4 * (j & 7));
