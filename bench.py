@@ -48,8 +48,8 @@ UNIT = "tokens/s"
 E2E_CHUNK_LAYERS = 2
 
 NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (184.295680e6 + 91.785984e6),
-                  "umma_distance_topk": 8 * (164.407808e6 + 4.297216e6),
-                  "umma_z_quant": 8 * (121.773824e6 + 3.546112e6),
+                  "umma_distance_topk": 8 * (164.111872e6 + 4.239872e6),
+                  "umma_z_quant": 8 * (121.798400e6 + 3.935488e6),
                   "umma_ref_proj": 8 * (50.373120e6 + 2.918656e6)}
 
 
