@@ -196,6 +196,20 @@ __device__ __forceinline__ float min3f(float a, float b, float c)
     asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
+// max of three that returns NaN if any input is NaN
+__device__ __forceinline__ float max3f_nan(float a, float b, float c)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// bits [0, len) of a inserted into b at bit pos
+__device__ __forceinline__ uint32_t bfi32(uint32_t a, uint32_t b, int pos, int len)
+{
+    uint32_t r;
+    asm("bfi.b32 %0, %1, %2, %3, %4;" : "=r"(r) : "r"(a), "r"(b), "r"(pos), "r"(len));
+    return r;
+}
 __device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, uint32_t (&w)[4],
                                               float &zmin, float &delta)
 {
@@ -222,22 +236,41 @@ __device__ __forceinline__ void quant_group32(const float (&v)[32], int bits, ui
     // 2^-24 relative and the quotient is at most 15, within 2^-20 of its rounding); so
     // where |r| is at least 2^-17 short of 1/2, RN(d/delta) is more than 2^-18 away from
     // the half-integer where floor(. + 1/2) changes, the rounding of RN(d/delta) + 1/2
-    // (at most 2^-20) cannot cross it, and q = round(x).  Nearer than that (and where
-    // delta is too small for a finite reciprocal) the correctly rounded division decides.
+    // (at most 2^-20) cannot cross it, and q = round(x) (in [0, 2^b - 1]: 0 <= x <=
+    // (2^b - 1)(1 + 2^-22)).  If any coordinate of the group is nearer than that (or delta
+    // is too small for a finite reciprocal) the correctly rounded division decides them all.
     const float rdl = __frcp_rn(dl);
-    const bool fast = dl >= 0x1p-100f;
     constexpr float kMagic = 12582912.0f;     // 1.5 * 2^23
+    // fast path, two coordinates per packed operation: t = x + 1.5 2^23 rounded, whose low
+    // mantissa bits are round(x); r = x - round(x) = x + (1.5 2^23 - t); the group takes
+    // this path when every |r| is at least 2^-17 short of 1/2
+    const float2 nlo = make_float2(-lo, -lo), rdl2 = make_float2(rdl, rdl);
+    const float2 mg = make_float2(kMagic, kMagic);
+    float rmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 d = __fadd2_rn(make_float2(v[j], v[j + 1]), nlo);
+        const float2 t = __ffma2_rn(d, rdl2, mg);
+        const float2 nq = __fadd2_rn(mg, make_float2(-t.x, -t.y));
+        const float2 r = __ffma2_rn(d, rdl2, nq);
+        rmax = max3f_nan(rmax, fabsf(r.x), fabsf(r.y));   // a NaN input takes the exact path
+        const uint32_t q0 = __float_as_uint(t.x), q1 = __float_as_uint(t.y);   // code in the low bits
+        if (bits == 4) {
+            w[j >> 3] = bfi32(q0, w[j >> 3], 4 * (j & 7), 4);
+            w[j >> 3] = bfi32(q1, w[j >> 3], 4 * ((j + 1) & 7), 4);
+        } else {
+            w[j >> 4] = bfi32(q0, w[j >> 4], 2 * (j & 15), 2);
+            w[j >> 4] = bfi32(q1, w[j >> 4], 2 * ((j + 1) & 15), 2);
+        }
+    }
+    if (dl >= 0x1p-100f && rmax <= 0.5f - 0x1p-17f) return;
+    // near a tie somewhere in the group (or delta too small for a finite reciprocal): the
+    // correctly rounded division for every coordinate
+    w[0] = w[1] = w[2] = w[3] = 0u;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        const float d = __fsub_rn(v[j], lo);
-        const float t = __fmaf_rn(d, rdl, kMagic);
-        const float qf = __fsub_rn(t, kMagic);                 // round(x), exact
-        const float r = __fmaf_rn(d, rdl, -qf);
-        int q = __float_as_int(t) - __float_as_int(kMagic);
-        if (!fast || fabsf(r) > 0.5f - 0x1p-17f) {
-            const float u = __fadd_rn(__fdiv_rn(d, dl), 0.5f);
-            q = (int)floorf(u);
-        }
+        const float u = __fadd_rn(__fdiv_rn(__fsub_rn(v[j], lo), dl), 0.5f);
+        int q = (int)floorf(u);
         q = q < 0 ? 0 : (q > qmax ? qmax : q);
         if (bits == 4)
             w[j >> 3] |= (uint32_t)q << (4 * (j & 7));
