@@ -480,11 +480,14 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 tile_pool = a.pool_size[min(a.T, (it.t + 1) * 2 * kBM) - 1];
             }
             bool is_ref = true;
-            if (MODE == M_S2) is_ref = in ? (a.ref_slot[tokr] >= 0) : true;
+            // a reference token or an exact copy of its references has z = 0 (S1 leaves
+            // its dh rows as they come)
+            if (MODE == M_S2)
+                is_ref = in ? (a.ref_slot[tokr] >= 0 || a.copy_flag[(size_t)it.lb * a.T + tokr] != 0) : true;
             if (MODE == M_S1) {
                 // this warp's 64 tokens: row offsets of the chosen references' projection
-                // rows (unused places point at the all-zero row), 1/k and a live flag,
-                // prepared in shared memory while the accumulator fills
+                // rows (unused places point at the all-zero row) and 1/k, prepared in
+                // shared memory while the accumulator fills
                 int4 *info = info_buf + (warp - 2) * 128;
                 const int tok0 = it.t * 2 * kBM + h * kHalfN + (q < 2 ? 0 : 64);
                 const int zoff = a.LB * a.n_ref * a.d_ff;
@@ -503,7 +506,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         ix = a.ref_idx[(size_t)it.lb * a.T + tj];
                     }
                     int4 o = make_int4(zoff, zoff, zoff, zoff);
-                    float inv_k = 0.0f, live = 0.0f;
+                    float inv_k = 0.0f;
                     if (rs < 0 && !cf) {
                         int kk = 0;
                         if (ix.x >= 0) { o.x = (lboff + ix.x) * a.d_ff; ++kk; }
@@ -511,12 +514,11 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (ix.z >= 0) { o.z = (lboff + ix.z) * a.d_ff; ++kk; }
                         if (ix.w >= 0) { o.w = (lboff + ix.w) * a.d_ff; ++kk; }
                         inv_k = kk > 0 ? 1.0f / (float)kk : 0.0f;
-                        live = 1.0f;
                     }
                     info[2 * j] = o;
-                    // 1/k for a live token (0 when its pool is empty), -1 for a reference
-                    // token or an exact copy (dh = 0)
-                    info[2 * j + 1] = make_int4(__float_as_int(live > 0.0f ? inv_k : -1.0f), 0, 0, 0);
+                    // 1/k (0 when the pool is empty, and for a reference token or an exact
+                    // copy, whose z the W_c3 pass sets to 0)
+                    info[2 * j + 1] = make_int4(__float_as_int(inv_k), 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -650,7 +652,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // rounds ahead of the arithmetic (a ring of three register buffers; the
                     // loop below is unrolled so that every buffer index is static)
                     float2 pr3[3][kS1Round][4];
-                    float sc3[3][kS1Round];                // 1/k for a live token, else -1
+                    float sc3[3][kS1Round];                // 1/k of each token
                     auto gather = [&](int c, float2 (&pr)[kS1Round][4], float (&sc)[kS1Round]) {
 #pragma unroll
                         for (int u = 0; u < kS1Round; ++u) {
@@ -666,8 +668,8 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // u / (1 + e^-u) over one reciprocal of both denominators:
                     //   dh = (g1 g2 (1 + e_m) - m1 m2 (1 + e_g)) / ((1 + e_g)(1 + e_m));
                     // e^-u is clamped at 2^63 (u < -43.6: Swish is below 1e-17 there) so
-                    // the denominator stays finite.  A reference token or an exact copy
-                    // has scale -1, so dh = 0.
+                    // the denominator stays finite.  The dh of a reference token or an
+                    // exact copy is not used: the W_c3 pass sets its z to 0.
                     auto finish = [&](int c, const float (&v)[kXTok], int v0, const float *xr,
                                       const float2 (&pr)[kS1Round][4], const float (&sc)[kS1Round]) {
                         __nv_bfloat16 *hi = a.dh_hi + ((size_t)it.lb * a.dh_rows + drow0) * a.d_ff + f;
@@ -678,8 +680,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const float g1 = gate ? v[v0 + u] : pv, g2 = gate ? pv : v[v0 + u];
                             const float2 s01 = __fadd2_rn(pr[u][0], pr[u][1]);
                             const float2 s23 = __fadd2_rn(pr[u][2], pr[u][3]);
-                            const float ik = fmaxf(sc[u], 0.0f);
-                            const float2 m = __fmul2_rn(__fadd2_rn(s01, s23), make_float2(ik, ik));
+                            const float2 m = __fmul2_rn(__fadd2_rn(s01, s23), make_float2(sc[u], sc[u]));
                             const float2 t = __fmul2_rn(make_float2(g1, m.x),
                                                         make_float2(-1.4426950408889634f, -1.4426950408889634f));
                             const float eg = exp2f_fast(fminf(t.x, 63.0f));
@@ -687,8 +688,7 @@ k_umma(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             const float2 d = __fadd2_rn(make_float2(eg, em), make_float2(1.0f, 1.0f));
                             const float2 pq = __fmul2_rn(make_float2(g1, m.x), make_float2(g2, m.y));
                             const float num = fmaf(pq.x, d.y, -(pq.y * d.x));
-                            const float live = sc[u] >= 0.0f ? 1.0f : 0.0f;
-                            const float dh = num * rcp_fast(d.x * d.y) * live;
+                            const float dh = num * rcp_fast(d.x * d.y);
                             const __nv_bfloat16 hb = __float2bfloat16_rn(dh);
                             if (fok && drow0 + c + u < a.dh_rows) {
                                 hi[(size_t)(c + u) * a.d_ff] = hb;
