@@ -47,9 +47,9 @@ UNIT = "tokens/s"
 # layers per chunk of the end-to-end step (copies of one chunk overlap another's compute)
 E2E_CHUNK_LAYERS = 2
 
-NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (184.295680e6 + 91.785984e6),
+NCU_DRAM_BYTES = {"umma_swiglu_diff": 8 * (183.950080e6 + 91.849984e6),
                   "umma_distance_topk": 8 * (164.111872e6 + 4.239872e6),
-                  "umma_z_quant": 8 * (121.798400e6 + 3.935488e6),
+                  "umma_z_quant": 8 * (121.788416e6 + 3.854080e6),
                   "umma_ref_proj": 8 * (50.373120e6 + 2.918656e6)}
 
 
