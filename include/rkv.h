@@ -43,7 +43,7 @@ extern "C" {
 typedef enum rkv_status {
     RKV_OK = 0,
     RKV_ERR_INVALID_ARG = 1,     /* null pointer, bad size or inconsistent params   */
-    RKV_ERR_UNSUPPORTED = 2,     /* valid for the method, not handled by this build */
+    RKV_ERR_UNSUPPORTED = 2,     /* valid for the method, not handled by this library */
     RKV_ERR_ALIGNMENT = 3,       /* a buffer is not 16-byte aligned                  */
     RKV_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed             */
     RKV_ERR_INDEX = 5,           /* device-detected: index out of range              */
