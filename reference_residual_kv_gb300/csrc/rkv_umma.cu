@@ -177,12 +177,6 @@ __device__ __forceinline__ float rcp_fast(float x)
     return y;
 }
 
-// Swish with a fast division (relative error ~1e-7, far inside the z tolerance)
-__device__ __forceinline__ float silu_fast(float u)
-{
-    return __fdividef(u, 1.0f + __expf(-u));
-}
-
 // kG > 0: every position that is 0 mod kG is a reference (fixed stride dividing kG,
 // first reference at 0), where dh = 0 and the record is all zero.
 //   S1: those token rows are not loaded: tmB is then a [LB][T/kG][kG][W] view, each CTA's

@@ -173,15 +173,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
         : "memory");
 }
 
-// Same, arriving on the mbarrier at `bar`'s offset in every CTA named in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
 // 32 consecutive fp32 accumulator columns of this thread's TMEM lane; the wait sits in
 // the same asm block so that no use of the outputs can be scheduled before it.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
