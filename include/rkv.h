@@ -136,7 +136,8 @@ rkv_status rkv_build_ref_pool(const rkv_params *p, const void *kv, const rkv_ref
  *  one allocation, the two gate halves load as one tile per pipeline stage, which is
  *  faster; any other placement is equally correct.)
  * workspace: >= workspace_bytes from rkv_query_sizes, 256-byte aligned.
- * z_out (nullable): [L*B][T][d_c] fp32 unquantised z (0 for reference tokens).
+ * z_out (nullable): [L*B][T][d_c] fp32 unquantised z (0 for reference tokens and for
+ * tokens equal to all their chosen references).
  * dev_status: device int32, set to RKV_OK by the caller.                         */
 rkv_status rkv_compress(const rkv_params *p, const void *kv, const rkv_ref_pool *pool,
                         const void *W1t, const void *W2t, const void *W3t,
