@@ -6,6 +6,7 @@ librkv.so is missing or cannot be loaded, every call raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -245,10 +246,40 @@ def rkv_profile_collect(max_entries: int = 64, name_len: int = 48):
 _TORCH_REF = {RKV_F32: torch.float32, RKV_BF16: torch.bfloat16, RKV_FP8_E4M3: torch.uint8}
 
 
-class Buffers:
-    """Caller-owned device buffers for one rkv_params: pool, cache, workspace, status."""
+GUARD_BYTE = 0xA5
 
-    def __init__(self, p: rkv_params, device="cuda", want_z: bool = False):
+
+def guarded_empty(shape, dtype, device, guard: int, fill=None):
+    """(tensor, raw): an uninitialised tensor of `shape` that is the head of a byte
+    allocation followed by `guard` bytes of GUARD_BYTE (guard = 0: a plain allocation,
+    raw is None).  A write past the tensor's end changes the tail (see guard_intact)."""
+    if guard <= 0:
+        t = torch.empty(shape, dtype=dtype, device=device)
+        if fill is not None:
+            t.fill_(fill)
+        return t, None
+    n = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+    raw = torch.empty(n + guard, dtype=torch.uint8, device=device)
+    raw[n:].fill_(GUARD_BYTE)
+    t = raw[:n].view(dtype).view(shape)
+    if fill is not None:
+        t.fill_(fill)
+    return t, raw
+
+
+def guard_intact(t, raw) -> bool:
+    if raw is None:
+        return True
+    n = t.numel() * t.element_size()
+    return bool((raw[n:] == GUARD_BYTE).all().item())
+
+
+class Buffers:
+    """Caller-owned device buffers for one rkv_params: pool, cache, workspace, status.
+    guard > 0 puts that many guard bytes after every buffer (test support: the tails are
+    checked by guard_violations())."""
+
+    def __init__(self, p: rkv_params, device="cuda", want_z: bool = False, guard: int = 0):
         self.p = p
         LB, T, W = p.L * p.B, p.T, 2 * p.N * p.D
         R = rkv_n_ref(p)
@@ -256,19 +287,27 @@ class Buffers:
             raise RkvError(RKV_ERR_INVALID_ARG, "Buffers")
         self.n_ref = R
         _, _, ws = rkv_query_sizes(p)
-        i32 = dict(dtype=torch.int32, device=device)
-        self.ref_pos = torch.empty(max(R, 1), **i32)
-        self.ref_slot = torch.empty(T, **i32)
-        self.pool_size = torch.empty(T, **i32)
-        self.ref_vec = torch.empty((LB, max(R, 1), W), dtype=_TORCH_REF[p.ref_dtype], device=device)
-        self.ref_sqnorm = torch.empty((LB, max(R, 1)), dtype=torch.float32, device=device)
-        self.codes = torch.empty((LB, T, p.d_c * p.bits // 8), dtype=torch.uint8, device=device)
-        self.hdr = torch.empty((LB, T, p.d_c // 32, 2), dtype=torch.float32, device=device)
-        self.ref_idx = torch.empty((LB, T, 4), **i32)
+        self.guard = guard
+        self._raw = {}
+
+        def alloc(name, shape, dtype, fill=None):
+            t, raw = guarded_empty(shape, dtype, device, guard, fill)
+            self._raw[name] = raw
+            return t
+
+        i32 = torch.int32
+        self.ref_pos = alloc("ref_pos", (max(R, 1),), i32)
+        self.ref_slot = alloc("ref_slot", (T,), i32)
+        self.pool_size = alloc("pool_size", (T,), i32)
+        self.ref_vec = alloc("ref_vec", (LB, max(R, 1), W), _TORCH_REF[p.ref_dtype])
+        self.ref_sqnorm = alloc("ref_sqnorm", (LB, max(R, 1)), torch.float32)
+        self.codes = alloc("codes", (LB, T, p.d_c * p.bits // 8), torch.uint8)
+        self.hdr = alloc("hdr", (LB, T, p.d_c // 32, 2), torch.float32)
+        self.ref_idx = alloc("ref_idx", (LB, T, 4), i32)
         self.workspace_bytes = ws
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
-        self.status = torch.zeros(4, **i32)
-        self.z = torch.empty((LB, T, p.d_c), dtype=torch.float32, device=device) if want_z else None
+        self.workspace = alloc("workspace", (max(ws, 256),), torch.uint8)
+        self.status = alloc("status", (4,), i32, fill=0)
+        self.z = alloc("z", (LB, T, p.d_c), torch.float32) if want_z else None
         self.pool = rkv_ref_pool(_ptr(self.ref_pos), _ptr(self.ref_slot), _ptr(self.pool_size),
                                  _ptr(self.ref_vec), _ptr(self.ref_sqnorm))
         self.cache = rkv_cache(_ptr(self.codes), _ptr(self.hdr), _ptr(self.ref_idx))
@@ -299,9 +338,19 @@ class Buffers:
         n_sel = sel.shape[-1]
         need = rkv_attention_workspace(self.p, H, n_sel)
         if getattr(self, "_attn_ws", None) is None or self._attn_ws.numel() < need:
-            self._attn_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.status.device)
+            self._attn_ws, self._raw["attention_workspace"] = guarded_empty(
+                (max(need, 256),), torch.uint8, self.status.device, self.guard)
         rkv_sparse_attention(self.p, H, q, k_hat, v_hat, sel, n_sel, out, self._attn_ws,
                              self._attn_ws.numel(), stream)
 
     def device_status(self) -> int:
         return int(self.status[0].item())
+
+    def guard_violations(self):
+        """Names of the buffers whose guard bytes changed (empty without guards)."""
+        bad = []
+        for name, raw in self._raw.items():
+            t = self._attn_ws if name == "attention_workspace" else getattr(self, name)
+            if raw is not None and t is not None and not guard_intact(t, raw):
+                bad.append(name)
+        return bad

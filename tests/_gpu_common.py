@@ -48,11 +48,36 @@ def to_device(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
 
 
+# Guard bytes after every device buffer the GPU tests hand to the library: a write past a
+# buffer's end changes them (checked by assert_guards and Buffers.guard_violations).
+GUARD = 4096
+_guarded = []
+
+
+def out_buffer(shape, dtype):
+    """An uninitialised device output tensor followed by GUARD guard bytes."""
+    t, raw = rkv.guarded_empty(tuple(shape), dtype, "cuda", GUARD)
+    _guarded.append((t, raw))
+    return t
+
+
+def assert_guards(*bufs):
+    """Every out_buffer since the last call, and every given Buffers, still has intact
+    guard bytes."""
+    torch.cuda.synchronize()
+    bad = [i for i, (t, raw) in enumerate(_guarded) if not rkv.guard_intact(t, raw)]
+    _guarded.clear()
+    assert not bad, "writes past the end of output buffers %s" % bad
+    for b in bufs:
+        v = b.guard_violations()
+        assert not v, "writes past the end of %s" % v
+
+
 def run_gpu(cfg: wl.Config, kv, w, want_z=True):
     """Build pool + compress through the C ABI; returns (Buffers, device inputs)."""
     ensure_lib()
     p = rkv.params_from_config(cfg)
-    bufs = rkv.Buffers(p, want_z=want_z)
+    bufs = rkv.Buffers(p, want_z=want_z, guard=GUARD)
     kv_d = to_device(np.stack(kv), cfg.kv_dtype)
     W1 = to_device(np.stack([x[0] for x in w]), cfg.kv_dtype)
     W2 = to_device(np.stack([x[1] for x in w]), cfg.kv_dtype)
@@ -60,6 +85,7 @@ def run_gpu(cfg: wl.Config, kv, w, want_z=True):
     bufs.build_ref_pool(kv_d)
     bufs.compress(kv_d, W1, W2, W3)
     torch.cuda.synchronize()
+    assert_guards(bufs)
     return bufs, (kv_d, W1, W2, W3)
 
 

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from reference_residual_kv_gb300 import build, rkv
 
@@ -130,3 +131,16 @@ def test_timeout_hook_validates_host_side(lib):
     # the timeout-path test hook checks its arguments on the host (no GPU needed)
     for cycles, skip in ((0, 0), (9999, 0), (3 * 10 ** 9, 0), (200000, -1)):
         assert lib.rkv_debug_wait_fault(cycles, skip) == rkv.RKV_ERR_INVALID_ARG
+
+
+def test_guard_bytes_detect_a_write_past_the_end():
+    # the test-support allocator behind the GPU tests' overrun checks, on host memory
+    t, raw = rkv.guarded_empty((3, 5), torch.float32, "cpu", 64)
+    t.fill_(1.0)
+    assert rkv.guard_intact(t, raw)
+    raw[t.numel() * t.element_size()] = 0          # the first byte past the tensor
+    assert not rkv.guard_intact(t, raw)
+    s, raw_s = rkv.guarded_empty((4,), torch.int32, "cpu", 16, fill=0)
+    assert torch.equal(s, torch.zeros(4, dtype=torch.int32)) and rkv.guard_intact(s, raw_s)
+    u, none = rkv.guarded_empty((2,), torch.uint8, "cpu", 0)
+    assert none is None and rkv.guard_intact(u, none)

@@ -10,7 +10,7 @@ import oracle
 import rkv_workload as wl
 from reference_residual_kv_gb300 import rkv
 
-from _gpu_common import ensure_lib, to_device
+from _gpu_common import GUARD, assert_guards, ensure_lib, out_buffer, to_device
 from test_gpu_restore import load_records, refs_f64
 
 pytestmark = pytest.mark.gpu
@@ -26,12 +26,13 @@ def _attend(cfg, q_bits, k_bits, v_bits, sel):
     ensure_lib()
     p = rkv.params_from_config(cfg)
     LB = cfg.L * cfg.B
-    out = torch.empty((LB, cfg.H, cfg.D), dtype=torch.float32, device="cuda")
+    out = out_buffer((LB, cfg.H, cfg.D), torch.float32)
     n_sel = sel.shape[1]
-    ws = torch.empty(max(rkv.rkv_attention_workspace(p, cfg.H, n_sel), 256), dtype=torch.uint8, device="cuda")
+    ws = out_buffer((max(rkv.rkv_attention_workspace(p, cfg.H, n_sel), 256),), torch.uint8)
     rkv.rkv_sparse_attention(p, cfg.H, _bf16(q_bits), _bf16(k_bits), _bf16(v_bits),
                              torch.from_numpy(sel.astype(np.int32)).cuda(), n_sel, out, ws, ws.numel())
     torch.cuda.synchronize()
+    assert_guards()
     return out.cpu().numpy()
 
 
@@ -86,21 +87,22 @@ def test_restore_then_attention_matches_the_oracle_chain():
     cfg = C["llama3.1-8b-kv"].replace(L=1, T=8192)
     ensure_lib()
     p = rkv.params_from_config(cfg)
-    bufs = rkv.Buffers(p)
+    bufs = rkv.Buffers(p, guard=GUARD)
     rec = wl.synthetic_records(cfg, bufs.n_ref, 0)
     load_records(cfg, bufs, [rec])
     Wd = wl.decoder_weights(cfg, 0)
     sel = np.sort(np.random.default_rng(3).choice(cfg.T, 2000, replace=False)).astype(np.int32)[None]
     dk = cfg.N * cfg.D
     sel_d = torch.from_numpy(sel).cuda()
-    out_k = torch.empty((1, sel.shape[1], dk), dtype=torch.bfloat16, device="cuda")
-    out_v = torch.empty_like(out_k)
+    out_k = out_buffer((1, sel.shape[1], dk), torch.bfloat16)
+    out_v = out_buffer(out_k.shape, out_k.dtype)
     bufs.restore(to_device(Wd[None], cfg.kv_dtype), sel_d, out_k, out_v, cfg.rope_base)
     q = wl.decode_queries(cfg, 0, 0)
-    out = torch.empty((1, cfg.H, cfg.D), dtype=torch.float32, device="cuda")
+    out = out_buffer((1, cfg.H, cfg.D), torch.float32)
     bufs.attend(cfg.H, _bf16(q), out_k, out_v, sel_d, out)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    assert_guards(bufs)
     q_, zmin, delta, idx, refs = rec
     K, V = oracle.restore(cfg, refs_f64(cfg, refs), q_, zmin, delta, idx,
                           wl.stored_to_f64(Wd, cfg.kv_dtype), sel[0])

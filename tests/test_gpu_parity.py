@@ -14,8 +14,8 @@ import oracle
 import rkv_workload as wl
 from reference_residual_kv_gb300 import rkv
 
-from _gpu_common import (CODE_BUDGET, check_all_indices, check_tokens, gen_inputs, host_records,
-                         run_gpu, sample_tokens, to_device)
+from _gpu_common import (CODE_BUDGET, assert_guards, check_all_indices, check_tokens, gen_inputs,
+                         host_records, out_buffer, run_gpu, sample_tokens, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -235,11 +235,12 @@ def test_gather_matches_oracle_read(name, out):
     n_sel = len(sels[0])
     sel = torch.tensor(np.stack(sels), dtype=torch.int32, device="cuda")
     odt = torch.float32 if out == "f32" else torch.bfloat16
-    out_z = torch.empty((LB, n_sel, cfg.d_c), dtype=odt, device="cuda")
-    out_m = torch.empty((LB, n_sel, cfg.W), dtype=odt, device="cuda")
+    out_z = out_buffer((LB, n_sel, cfg.d_c), odt)
+    out_m = out_buffer((LB, n_sel, cfg.W), odt)
     bufs.gather(sel, out_z, out_m)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    assert_guards(bufs)
     gz = out_z.float().cpu().numpy()
     gm = out_m.float().cpu().numpy()
     for lb in range(LB):
@@ -295,13 +296,13 @@ def test_gather_standalone_padding_and_isolation():
     T = cfg.T
     # standalone mode (every token) equals the union of sparse reads
     allsel = torch.arange(T, dtype=torch.int32, device="cuda").view(1, T)
-    za = torch.empty((1, T, cfg.d_c), dtype=torch.bfloat16, device="cuda")
-    ma = torch.empty((1, T, cfg.W), dtype=torch.bfloat16, device="cuda")
+    za = out_buffer((1, T, cfg.d_c), torch.bfloat16)
+    ma = out_buffer((1, T, cfg.W), torch.bfloat16)
     bufs.gather(allsel, za, ma)
     sel_np = wl.gather_selection(cfg, 0)
     sel = torch.tensor(np.concatenate([sel_np, [-1, -1, -1]]), dtype=torch.int32, device="cuda").view(1, -1)
-    zs = torch.empty((1, sel.shape[1], cfg.d_c), dtype=torch.bfloat16, device="cuda")
-    ms = torch.empty((1, sel.shape[1], cfg.W), dtype=torch.bfloat16, device="cuda")
+    zs = out_buffer((1, sel.shape[1], cfg.d_c), torch.bfloat16)
+    ms = out_buffer((1, sel.shape[1], cfg.W), torch.bfloat16)
     bufs.gather(sel, zs, ms)
     torch.cuda.synchronize()
     idx = torch.tensor(sel_np, device="cuda", dtype=torch.long)
@@ -313,11 +314,12 @@ def test_gather_standalone_padding_and_isolation():
     bufs.codes[0, other] = 0xFF
     bufs.hdr[0, other] = float("nan")
     bufs.ref_idx[0, other] = 1 << 30
-    zp, mp = torch.empty_like(zs), torch.empty_like(ms)
+    zp, mp = out_buffer(zs.shape, zs.dtype), out_buffer(ms.shape, ms.dtype)
     bufs.gather(sel, zp, mp)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
     assert torch.equal(zp, zs) and torch.equal(mp, ms)
+    assert_guards(bufs)
 
 
 @pytest.mark.parametrize("name", ["tiny-fp32", "long-fp8-1x1500"])
@@ -349,11 +351,12 @@ def test_long_context_decode_steps():
     for step in range(3):
         s = wl.gather_selection(cfg, step)
         sel = torch.tensor(s, dtype=torch.int32, device="cuda").view(1, -1)
-        oz = torch.empty((1, s.size, cfg.d_c), dtype=torch.bfloat16, device="cuda")
-        om = torch.empty((1, s.size, cfg.W), dtype=torch.bfloat16, device="cuda")
+        oz = out_buffer((1, s.size, cfg.d_c), torch.bfloat16)
+        om = out_buffer((1, s.size, cfg.W), torch.bfloat16)
         bufs.gather(sel, oz, om)
         torch.cuda.synchronize()
         assert bufs.device_status() == 0
+        assert_guards(bufs)
         pick = np.sort(np.concatenate([np.random.default_rng(step).choice(s.size - 512, 40, replace=False),
                                        s.size - 1 - np.arange(8)]))
         _check_read(cfg, kv[0][0], gpu, 0, s[pick], oz[0, pick].float().cpu().numpy(),

@@ -15,7 +15,7 @@ import oracle
 import rkv_workload as wl
 from reference_residual_kv_gb300 import rkv
 
-from _gpu_common import ensure_lib, gen_inputs, run_gpu, to_device
+from _gpu_common import GUARD, assert_guards, ensure_lib, gen_inputs, out_buffer, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -69,7 +69,7 @@ def compare_rows(got, want, what):
 def _restore_case(cfg, n_sel, seed):
     ensure_lib()
     p = rkv.params_from_config(cfg)
-    bufs = rkv.Buffers(p)
+    bufs = rkv.Buffers(p, guard=GUARD)
     n_ref = bufs.n_ref
     recs = [wl.synthetic_records(cfg, n_ref, lb) for lb in range(cfg.L * cfg.B)]
     load_records(cfg, bufs, recs)
@@ -80,11 +80,12 @@ def _restore_case(cfg, n_sel, seed):
     sel[:, -1] = cfg.T - 1                         # the largest position (widest RoPE angles)
     sel_d = torch.from_numpy(sel.astype(np.int32)).cuda()
     dk = cfg.N * cfg.D
-    out_k = torch.empty((cfg.L * cfg.B, n_sel, dk), dtype=torch.bfloat16, device="cuda")
-    out_v = torch.empty_like(out_k)
+    out_k = out_buffer((cfg.L * cfg.B, n_sel, dk), torch.bfloat16)
+    out_v = out_buffer(out_k.shape, out_k.dtype)
     bufs.restore(Wd_d, sel_d, out_k, out_v, cfg.rope_base)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    assert_guards(bufs)
     gk = out_k.float().cpu().numpy()
     gv = out_v.float().cpu().numpy()
     for lb, (q, zmin, delta, idx, refs) in enumerate(recs):
@@ -115,11 +116,12 @@ def test_restore_of_reference_tokens_in_a_written_cache():
     sel = np.arange(0, cfg.T, s, dtype=np.int32)[:100]
     Wd_d = to_device(wl.decoder_weights(cfg, 0)[None], cfg.kv_dtype)
     dk = cfg.N * cfg.D
-    out_k = torch.empty((1, sel.size, dk), dtype=torch.bfloat16, device="cuda")
-    out_v = torch.empty_like(out_k)
+    out_k = out_buffer((1, sel.size, dk), torch.bfloat16)
+    out_v = out_buffer(out_k.shape, out_k.dtype)
     bufs.restore(Wd_d, torch.from_numpy(sel[None]).cuda(), out_k, out_v, cfg.rope_base)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    assert_guards(bufs)
     x = kv[0][0][sel]                                    # bf16 bits [n][W]
     assert np.array_equal(out_v[0].cpu().view(torch.int16).numpy().view(np.uint16), x[:, dk:])
     xk = wl.stored_to_f64(x[:, :dk], "bf16")
@@ -166,19 +168,20 @@ def test_restore_full_size_sampled():
     cfg = C["long-131k-fp8ref"]
     ensure_lib()
     p = rkv.params_from_config(cfg)
-    bufs = rkv.Buffers(p)
+    bufs = rkv.Buffers(p, guard=GUARD)
     rec = wl.synthetic_records(cfg, bufs.n_ref, 0)
     load_records(cfg, bufs, [rec])
     Wd = wl.decoder_weights(cfg, 0)
     sel = wl.gather_selection(cfg, 0).astype(np.int32)[None]
     n = sel.shape[1]
     dk = cfg.N * cfg.D
-    out_k = torch.empty((1, n, dk), dtype=torch.bfloat16, device="cuda")
-    out_v = torch.empty_like(out_k)
+    out_k = out_buffer((1, n, dk), torch.bfloat16)
+    out_v = out_buffer(out_k.shape, out_k.dtype)
     bufs.restore(to_device(Wd[None], cfg.kv_dtype), torch.from_numpy(sel).cuda(), out_k, out_v,
                  cfg.rope_base)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    assert_guards(bufs)
     pick = np.sort(np.random.default_rng(11).choice(n, 64, replace=False))
     pick[-1] = n - 1                                     # the last position
     q, zmin, delta, idx, refs = rec
